@@ -1,0 +1,369 @@
+/*
+ * dspark_oracle.c -- CPU oracle for DSpark ancestral draft-block sampling.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file: only tests/, __graft_entry__.smoke() and bench.py's
+ * cpu_baseline / reference legs use it.  It shares no code, header, table or
+ * constant generator with the CUDA path under ancestral_draft_sampling_gb300/.
+ *
+ * A plain, slow, obviously-correct restatement of what the method computes,
+ * in the order the pages state it:
+ *
+ *   brb-nv/TensorRT-LLM PR #21, "2. Golden sampling semantics":
+ *     position k is drawn from softmax((base_k + bias(d_{k-1})) / T), where
+ *     d_{k-1} is the token drawn just before it; drafts use the temperature
+ *     only (no top-k / top-p / min-p); greedy requests draft the argmax chain;
+ *     the distribution each draft was drawn from is stored as its proposal.
+ *   brb-nv/TensorRT-LLM PR #27, "2. One fused kernel per draft position":
+ *     add the Markov bias, scale by 1/T, take the argmax of the scaled logits
+ *     plus Gumbel noise from a counter-based Philox stream keyed by the
+ *     request's (seed, offset) draft slot of position k; biased logits are
+ *     kept in float32; afterwards q_k = softmax(logits_k / T) is written from
+ *     those float32 logits, recomputing logits_k / T bit for bit; CUDA-graph
+ *     padding rows draw from the bias alone.  Results table: the Markov head
+ *     is rank 256 ("rank-256 Markov head").
+ *   brb-nv/TensorRT-LLM PR #21, "2. Golden sampling semantics": the default
+ *     verification rule is standard token-level rejection sampling.
+ *
+ * Readings where the pages are silent (each is listed in the design doc):
+ *   - Philox variant: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
+ *     random numbers: as easy as 1, 2, 3", SC'11).
+ *   - Counter layout: key = (seed lo, seed hi); counter =
+ *     (v >> 2, k | stream << 16, offset lo, offset hi), word v & 3.
+ *     stream 0 = draft noise, 1 = acceptance uniforms, 2 = residual / bonus
+ *     noise.
+ *   - Gumbel transform: w = (x + 0.5) * 2^-32, g = -log(-log1p(-w)).
+ *   - The scaled logit is the float32 IEEE quotient l / T (pages: "bit for
+ *     bit").  The perturbed score that decides the token is taken in the
+ *     kernel's precision: g is computed in double and rounded once to float,
+ *     and score = s + g is a float32 addition.  Ties go to the lowest index;
+ *     a NaN score never wins.
+ *   - Greedy rows consume no noise and store a one-hot proposal (PR #27,
+ *     "Also checked": a greedy-sentinel row draws the argmax with a one-hot
+ *     proposal).
+ *   - Padding rows ignore the drafter logits (even NaN) and use l = bias.
+ *   - Bias: accumulated in double over j = 0..r-1, then l = base + bias is
+ *     rounded once to float.
+ *   - Verification uniforms: u = ((x >> 9) + 0.5) * 2^-23, exact in float;
+ *     accept iff float(u * q[d]) < p[d].
+ *
+ * Build: gcc -O2 -fPIC -shared -ffp-contract=off (no -ffast-math: IEEE float
+ * division and the libm log/exp are relied on).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* ---------------------------------------------------------------- Philox */
+
+/* Philox4x32-10, SC'11 paper: the round multipliers and the Weyl key
+ * increments are the published constants of the Philox-4x32 family. */
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+void oracle_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2],
+                          uint32_t out[4]) {
+  uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+  uint32_t k0 = key_in[0], k1 = key_in[1];
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) { /* the key is bumped between rounds */
+      k0 += PHILOX_W0;
+      k1 += PHILOX_W1;
+    }
+    uint64_t p0 = (uint64_t)PHILOX_M0 * (uint64_t)c0;
+    uint64_t p1 = (uint64_t)PHILOX_M1 * (uint64_t)c2;
+    uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+    uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+    uint32_t n0 = hi1 ^ c1 ^ k0;
+    uint32_t n1 = lo1;
+    uint32_t n2 = hi0 ^ c3 ^ k1;
+    uint32_t n3 = lo0;
+    c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+  }
+  out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* The raw 32-bit word that feeds element `index` of stream `stream` at
+ * position k of request (seed, offset). */
+uint32_t oracle_noise_word(uint64_t seed, uint64_t offset, int k, int stream,
+                           uint32_t index) {
+  uint32_t ctr[4], key[2], out[4];
+  ctr[0] = index >> 2;
+  ctr[1] = (uint32_t)k | ((uint32_t)stream << 16);
+  ctr[2] = (uint32_t)(offset & 0xffffffffu);
+  ctr[3] = (uint32_t)(offset >> 32);
+  key[0] = (uint32_t)(seed & 0xffffffffu);
+  key[1] = (uint32_t)(seed >> 32);
+  oracle_philox4x32_10(ctr, key, out);
+  return out[index & 3u];
+}
+
+/* Standard Gumbel variate from one 32-bit word: w uniform in (0, 1),
+ * g = -log(-log(1 - w)). */
+double oracle_gumbel(uint32_t x) {
+  double w = ((double)x + 0.5) * 0x1p-32;
+  double e = -log1p(-w);
+  return -log(e);
+}
+
+/* Uniform in (0, 1) for the acceptance test; exact in float and double. */
+float oracle_accept_uniform(uint32_t x) {
+  return (float)(((double)(x >> 9) + 0.5) * 0x1p-23);
+}
+
+/* ------------------------------------------------------------- helpers */
+
+static double load_elem(const void* p, int dtype, size_t i) {
+  if (dtype == ORACLE_F32) return (double)((const float*)p)[i];
+  uint32_t bits = (uint32_t)((const uint16_t*)p)[i] << 16;
+  float f;
+  memcpy(&f, &bits, sizeof f);
+  return (double)f;
+}
+
+/* ---------------------------------------------------- one draft position */
+
+/*
+ * One draft position of one request.
+ *
+ * base_row : [V] drafter logits of this (request, position), dtype base_dtype;
+ *            ignored when is_pad != 0 (may be NULL then).
+ * U        : [V, r] row-major, Wb : [r, V] row-major, both of dtype w_dtype.
+ * prev     : the token drawn just before this position (d0 for position 0).
+ * Outputs  : logits_out [V] float32 biased logits l,
+ *            probs_out [V] proposal q in double (one-hot for greedy rows),
+ *            *token_out, *M_out = max s, *S_out = sum exp(s - M),
+ *            *best_out / *second_out = the two largest decision scores
+ *            (float32 s + g for sampled rows, s for greedy rows; second is
+ *            the largest over v != token, -inf when V == 1).
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_draft_position(const void* base_row, int base_dtype, int is_pad,
+                          const void* U, const void* Wb, int w_dtype, int V,
+                          int r, int prev, uint64_t seed, uint64_t offset,
+                          int k, float T, int greedy, float* logits_out,
+                          double* probs_out, int* token_out, double* M_out,
+                          double* S_out, float* best_out, float* second_out,
+                          double* bias_scratch /* [V] */) {
+  if (V <= 0 || r <= 0 || prev < 0 || prev >= V || !(T > 0.0f) ||
+      !isfinite(T) || U == NULL || Wb == NULL || bias_scratch == NULL ||
+      (!is_pad && base_row == NULL))
+    return -1;
+
+  /* bias(d) = U[d] @ Wb, accumulated in double in the order j = 0..r-1 */
+  for (int v = 0; v < V; ++v) bias_scratch[v] = 0.0;
+  for (int j = 0; j < r; ++j) {
+    double u = load_elem(U, w_dtype, (size_t)prev * (size_t)r + (size_t)j);
+    for (int v = 0; v < V; ++v)
+      bias_scratch[v] += u * load_elem(Wb, w_dtype, (size_t)j * (size_t)V + v);
+  }
+
+  /* l = base + bias, rounded once to float; padding rows use the bias alone */
+  for (int v = 0; v < V; ++v) {
+    double base = is_pad ? 0.0 : load_elem(base_row, base_dtype, (size_t)v);
+    logits_out[v] = (float)(base + bias_scratch[v]);
+  }
+
+  /* decision: argmax of s (greedy) or of float(s + g) (sampled) */
+  int token = 0;
+  float best = -INFINITY;
+  int found = 0;
+  for (int v = 0; v < V; ++v) {
+    float s = logits_out[v] / T;
+    float score;
+    if (greedy) {
+      score = s;
+    } else {
+      float g = (float)oracle_gumbel(oracle_noise_word(seed, offset, k, 0,
+                                                       (uint32_t)v));
+      score = s + g;
+    }
+    if (isnan(score)) continue;
+    if (!found || score > best) {
+      best = score;
+      token = v;
+      found = 1;
+    }
+  }
+  float second = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    if (v == token) continue;
+    float s = logits_out[v] / T;
+    float score = s;
+    if (!greedy)
+      score = s + (float)oracle_gumbel(
+                      oracle_noise_word(seed, offset, k, 0, (uint32_t)v));
+    if (!isnan(score) && score > second) second = score;
+  }
+
+  /* proposal q = softmax(s) in double from the float32 s */
+  double M = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double s = (double)(logits_out[v] / T);
+    if (!isnan(s) && s > M) M = s;
+  }
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) S += exp((double)(logits_out[v] / T) - M);
+  if (greedy) {
+    for (int v = 0; v < V; ++v) probs_out[v] = (v == token) ? 1.0 : 0.0;
+  } else {
+    for (int v = 0; v < V; ++v)
+      probs_out[v] = exp((double)(logits_out[v] / T) - M) / S;
+  }
+
+  *token_out = token;
+  *M_out = M;
+  *S_out = S;
+  *best_out = found ? best : -INFINITY;
+  *second_out = second;
+  return 0;
+}
+
+/* ------------------------------------------------------- whole draft block */
+
+/*
+ * The ancestral draft block: for every request b, positions k = 0..K-1 in
+ * order, each conditioned on the token drawn before it (d0[b] for k = 0).
+ *
+ * base [B,K,V] (base_dtype), U [V,r], Wb [r,V] (w_dtype), d0/seed/offset [B],
+ * greedy/pad_row [B] or NULL.  force_tokens [B,K] or NULL: when given, the
+ * token that conditions position k+1 is force_tokens[b,k] instead of the
+ * oracle's own draw (used to follow another implementation's chain after an
+ * allowed near-tie disagreement); tokens[] still receives the oracle's draws.
+ * Outputs: tokens [B,K], logits [B,K,V] float32, probs [B,K,V] double,
+ * rowstats [B,K,2] (M, S) double, top2 [B,K,2] float (best, second) or NULL.
+ */
+int oracle_draft_block(const void* base, int base_dtype, const void* U,
+                       const void* Wb, int w_dtype, const int32_t* d0,
+                       const uint64_t* seed, const uint64_t* offset, float T,
+                       const uint8_t* greedy, const uint8_t* pad_row, int B,
+                       int K, int V, int r, const int32_t* force_tokens,
+                       int32_t* tokens, float* logits, double* probs,
+                       double* rowstats, float* top2, double* bias_scratch) {
+  if (B <= 0 || K <= 0) return -1;
+  size_t elt = (base_dtype == ORACLE_F32) ? 4 : 2;
+  for (int b = 0; b < B; ++b) {
+    int prev = d0[b];
+    int is_pad = pad_row ? pad_row[b] != 0 : 0;
+    int is_greedy = greedy ? greedy[b] != 0 : 0;
+    for (int k = 0; k < K; ++k) {
+      size_t row = (size_t)b * (size_t)K + (size_t)k;
+      const void* base_row =
+          is_pad ? NULL : (const char*)base + row * (size_t)V * elt;
+      int token;
+      double M, S;
+      float best, second;
+      int rc = oracle_draft_position(
+          base_row, base_dtype, is_pad, U, Wb, w_dtype, V, r, prev, seed[b],
+          offset[b], k, T, is_greedy, logits + row * (size_t)V,
+          probs + row * (size_t)V, &token, &M, &S, &best, &second,
+          bias_scratch);
+      if (rc) return rc;
+      tokens[row] = token;
+      if (rowstats) {
+        rowstats[2 * row] = M;
+        rowstats[2 * row + 1] = S;
+      }
+      if (top2) {
+        top2[2 * row] = best;
+        top2[2 * row + 1] = second;
+      }
+      prev = force_tokens ? force_tokens[row] : token;
+      if (prev < 0 || prev >= V) return -1;
+    }
+  }
+  return 0;
+}
+
+/* -------------------------------------------------- standard verification */
+
+/* Gumbel-max draw from the unnormalised weights w[0..V-1] >= 0 with stream 2
+ * noise at position kk: argmax of float(log w) + float(g), lowest index on
+ * ties, zero weights never win.  Returns -1 when every weight is zero. */
+static int gumbel_max_weights(const float* w, int V, uint64_t seed,
+                              uint64_t offset, int kk, float* best_out,
+                              float* second_out) {
+  int token = -1;
+  float best = -INFINITY, second = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    if (!(w[v] > 0.0f)) continue;
+    float lw = (float)log((double)w[v]);
+    float g = (float)oracle_gumbel(
+        oracle_noise_word(seed, offset, kk, 2, (uint32_t)v));
+    float score = lw + g;
+    if (token < 0 || score > best) {
+      if (token >= 0) second = best;
+      best = score;
+      token = v;
+    } else if (score > second) {
+      second = score;
+    }
+  }
+  if (best_out) *best_out = best;
+  if (second_out) *second_out = second;
+  return token;
+}
+
+/*
+ * Standard token-level rejection sampling (the default "standard" rule of
+ * PR #21, "2. Golden sampling semantics"; Leviathan et al. 2023, Chen et al.
+ * 2023).  For k = 0..K-1: draft d = tokens[b,k] is accepted iff
+ * float(u_k * q_k[d]) < p_k[d] with u_k uniform (stream 1, word 0).  At the
+ * first rejection the emitted token is drawn from norm(max(p_k - q_k, 0))
+ * (from p_k if that residual is all zero) and accepted_len = k; if all K are
+ * accepted the emitted token is drawn from the bonus row p_K and
+ * accepted_len = K.  Draws use Gumbel-max with stream 2 noise at position k
+ * (K for the bonus row).
+ *
+ * draft_probs [B,K,V], target_probs [B,K+1,V] float32, tokens [B,K].
+ * emit_top2 [B,2] or NULL receives the two largest scores of the emitting
+ * draw.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_verify_standard(const float* draft_probs, const float* target_probs,
+                           const int32_t* tokens, const uint64_t* seed,
+                           const uint64_t* offset, int B, int K, int V,
+                           int32_t* accepted_len, int32_t* emitted,
+                           float* emit_top2, float* residual_scratch) {
+  if (B <= 0 || K <= 0 || V <= 0) return -1;
+  for (int b = 0; b < B; ++b) {
+    int acc = K;
+    int emit = -1;
+    float best = -INFINITY, second = -INFINITY;
+    for (int k = 0; k < K; ++k) {
+      int d = tokens[(size_t)b * K + k];
+      if (d < 0 || d >= V) return -1;
+      const float* q = draft_probs + ((size_t)b * K + k) * (size_t)V;
+      const float* p = target_probs + ((size_t)b * (K + 1) + k) * (size_t)V;
+      float u = oracle_accept_uniform(
+          oracle_noise_word(seed[b], offset[b], k, 1, 0u));
+      float uq = u * q[d];
+      if (uq < p[d]) continue; /* accepted */
+      acc = k;
+      int any = 0;
+      for (int v = 0; v < V; ++v) {
+        float diff = p[v] - q[v];
+        residual_scratch[v] = diff > 0.0f ? diff : 0.0f;
+        if (residual_scratch[v] > 0.0f) any = 1;
+      }
+      const float* w = any ? residual_scratch : p;
+      emit = gumbel_max_weights(w, V, seed[b], offset[b], k, &best, &second);
+      break;
+    }
+    if (acc == K) {
+      const float* pK = target_probs + ((size_t)b * (K + 1) + K) * (size_t)V;
+      emit = gumbel_max_weights(pK, V, seed[b], offset[b], K, &best, &second);
+    }
+    accepted_len[b] = acc;
+    emitted[b] = emit < 0 ? 0 : emit;
+    if (emit_top2) {
+      emit_top2[2 * b] = best;
+      emit_top2[2 * b + 1] = second;
+    }
+  }
+  return 0;
+}
