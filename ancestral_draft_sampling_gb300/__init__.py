@@ -1,0 +1,182 @@
+"""GB300-native DSpark ancestral draft-block sampling.
+
+The sampler of brb-nv/TensorRT-LLM PR #27 ("2. One fused kernel per draft
+position") with the semantics of brb-nv/TensorRT-LLM PR #21 ("2. Golden
+sampling semantics"), as hand-written CUDA for sm_103a behind the C ABI in
+``include/dspark.h``.  This module is the thin PyTorch-facing binding: it
+takes torch tensors, checks dtypes and shapes, and passes raw pointers and
+the current CUDA stream to the library.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+from . import _lib
+from ._lib import BF16, F32, DsparkError  # noqa: F401
+
+__all__ = ["draft_block", "draft_block_profile", "verify_standard", "noise_words", "workspace_bytes",
+           "read_device_error", "DraftWorkspace", "DsparkError", "F32", "BF16",
+           "version"]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"expected float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def version() -> str:
+    return _lib.load().dspark_version().decode()
+
+
+def workspace_bytes(B: int, K: int, V: int, r: int) -> int:
+    return int(_lib.load().dspark_draft_workspace_bytes(B, K, V, r))
+
+
+class DraftWorkspace:
+    """Device scratch for dspark_draft_block, sized for (B, K, V, r)."""
+
+    def __init__(self, B: int, K: int, V: int, r: int, device=None):
+        torch = _torch()
+        n = workspace_bytes(B, K, V, r)
+        if n == 0:
+            raise DsparkError("dspark_draft_workspace_bytes", 2)
+        self.nbytes = n
+        # torch's caching allocator returns 512-byte aligned blocks
+        self.buffer = torch.empty(n, dtype=torch.uint8,
+                                  device=device or "cuda")
+
+
+def draft_block(base_logits, U, Wb, d0, seed, offset, T: float, *,
+                greedy=None, pad_row=None, tokens=None, logits=None,
+                draft_probs=None, workspace: Optional[DraftWorkspace] = None,
+                stream=None):
+    """Drafts one K-token block for B requests.  See include/dspark.h.
+
+    base_logits [B,K,V] float32|bfloat16, U [V,r], Wb [r,V] (same dtype),
+    d0 [B] int32, seed/offset [B] int64 (bit patterns of uint64),
+    greedy/pad_row [B] uint8 or None.  Returns (tokens, logits, draft_probs).
+    """
+    torch = _torch()
+    B, K, V = base_logits.shape
+    r = U.shape[1]
+    if tuple(U.shape) != (V, r) or tuple(Wb.shape) != (r, V):
+        raise ValueError("U must be [V, r] and Wb [r, V]")
+    if U.dtype != Wb.dtype:
+        raise TypeError("U and Wb must share a dtype")
+    for t in (base_logits, U, Wb, d0, seed, offset, greedy, pad_row):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    dev = base_logits.device
+    if tokens is None:
+        tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if logits is None:
+        logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if draft_probs is None:
+        draft_probs = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = DraftWorkspace(B, K, V, r, device=dev)
+    st = _lib.load().dspark_draft_block(
+        _ptr(base_logits), _dtype_code(base_logits), _ptr(U), _ptr(Wb),
+        _dtype_code(U), _ptr(d0), _ptr(seed), _ptr(offset), float(T),
+        _ptr(greedy), _ptr(pad_row), B, K, V, r, _ptr(tokens), _ptr(logits),
+        _ptr(draft_probs), _ptr(workspace.buffer), workspace.nbytes,
+        _stream(stream))
+    _lib.check("dspark_draft_block", st)
+    return tokens, logits, draft_probs
+
+
+def draft_block_profile(base_logits, U, Wb, d0, seed, offset, T: float, *,
+                        greedy=None, pad_row=None, tokens=None, logits=None,
+                        draft_probs=None, workspace=None, stream=None):
+    """dspark_draft_block_profile: runs one block with CUDA events around
+    every launch and returns {class: (total_ms, launches)} for the classes
+    "position", "pick" and "proposal" (synchronises; not capturable)."""
+    torch = _torch()
+    B, K, V = base_logits.shape
+    r = U.shape[1]
+    dev = base_logits.device
+    if tokens is None:
+        tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if logits is None:
+        logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if draft_probs is None:
+        draft_probs = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = DraftWorkspace(B, K, V, r, device=dev)
+    ms = (ctypes.c_float * 3)()
+    n = (ctypes.c_int * 3)()
+    st = _lib.load().dspark_draft_block_profile(
+        _ptr(base_logits), _dtype_code(base_logits), _ptr(U), _ptr(Wb),
+        _dtype_code(U), _ptr(d0), _ptr(seed), _ptr(offset), float(T),
+        _ptr(greedy), _ptr(pad_row), B, K, V, r, _ptr(tokens), _ptr(logits),
+        _ptr(draft_probs), _ptr(workspace.buffer), workspace.nbytes,
+        ctypes.cast(ms, ctypes.c_void_p), ctypes.cast(n, ctypes.c_void_p),
+        _stream(stream))
+    _lib.check("dspark_draft_block_profile", st)
+    names = ("position", "pick", "proposal")
+    return {names[i]: (float(ms[i]), int(n[i])) for i in range(3)}
+
+
+def verify_standard(draft_probs, target_probs, tokens, seed, offset, *,
+                    accepted_len=None, emitted_token=None, stream=None):
+    """Standard rejection verification.  Returns (accepted_len, emitted)."""
+    torch = _torch()
+    B, K, V = draft_probs.shape
+    if tuple(target_probs.shape) != (B, K + 1, V):
+        raise ValueError("target_probs must be [B, K+1, V]")
+    dev = draft_probs.device
+    if accepted_len is None:
+        accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if emitted_token is None:
+        emitted_token = torch.empty(B, dtype=torch.int32, device=dev)
+    st = _lib.load().dspark_verify_standard(
+        _ptr(draft_probs), _ptr(target_probs), _ptr(tokens), _ptr(seed),
+        _ptr(offset), B, K, V, _ptr(accepted_len), _ptr(emitted_token),
+        _stream(stream))
+    _lib.check("dspark_verify_standard", st)
+    return accepted_len, emitted_token
+
+
+def noise_words(seed: int, offset: int, k: int, stream_id: int, n: int,
+                device=None, with_gumbel: bool = True, stream=None):
+    """Diagnostic: the raw Philox words (and float32 Gumbel variates) the
+    kernels use for elements 0..n-1.  Returns (words int32-view, gumbel)."""
+    torch = _torch()
+    dev = device or "cuda"
+    out = torch.empty(n, dtype=torch.int32, device=dev)
+    g = torch.empty(n, dtype=torch.float32, device=dev) if with_gumbel else None
+    st = _lib.load().dspark_noise_words(seed, offset, k, stream_id, n,
+                                        _ptr(out), _ptr(g), _stream(stream))
+    _lib.check("dspark_noise_words", st)
+    return out, g
+
+
+def read_device_error(workspace: DraftWorkspace, stream=None) -> int:
+    """Reads and clears the workspace's device error word (synchronises)."""
+    code = ctypes.c_int(0)
+    st = _lib.load().dspark_read_device_error(
+        _ptr(workspace.buffer), ctypes.byref(code), _stream(stream))
+    if st not in (0, 5):
+        _lib.check("dspark_read_device_error", st)
+    return code.value

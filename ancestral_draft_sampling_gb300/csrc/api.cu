@@ -1,0 +1,281 @@
+// api.cu -- the C ABI declared in include/dspark.h: argument checks,
+// workspace layout and the launch sequence of one draft block.
+//
+// Launch sequence of dspark_draft_block (brb-nv/TensorRT-LLM PR #27,
+// "2. One fused kernel per draft position"): for k = 0..K-1, one position
+// kernel (bias, scaling, Gumbel-max, logits, chunk statistics) and one pick
+// kernel (token d_k, row max and sum-exp); then one proposal writer for all
+// positions.  2K+1 launches on the caller's stream, no host synchronisation,
+// so the whole call can be captured in a CUDA graph.
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "dspark_common.cuh"
+
+namespace dspark {
+int generic_chunks_used(int V, int n_chunks);
+}
+
+namespace {
+
+using namespace dspark;
+
+bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+bool sizes_supported(int B, int K, int V, int r) {
+  return B >= 1 && B <= DSPARK_MAX_B && K >= 1 && K <= DSPARK_MAX_K &&
+         V >= 1 && V <= DSPARK_MAX_V && r >= 16 && r <= DSPARK_MAX_R &&
+         r % 16 == 0;
+}
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        n <= 0)
+      n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  return n;
+}
+
+dspark_status from_cuda(cudaError_t e) {
+  return e == cudaSuccess ? DSPARK_OK : DSPARK_ERR_CUDA;
+}
+
+// Checks the arguments of dspark_draft_block and fills the kernel arguments.
+dspark_status prepare_draft(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, DraftArgs& a) {
+  // ---- argument checks, before any launch
+  if (B <= 0 || K <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (!base_logits || !U || !Wb || !d0 || !seed || !offset || !tokens ||
+      !logits || !draft_probs)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!(T > 0.0f) || !std::isfinite(T)) return DSPARK_ERR_INVALID_ARG;
+  if ((base_dtype != DSPARK_F32 && base_dtype != DSPARK_BF16) ||
+      (w_dtype != DSPARK_F32 && w_dtype != DSPARK_BF16))
+    return DSPARK_ERR_INVALID_ARG;
+  const void* ptrs[] = {base_logits, U, Wb, d0, seed, offset, tokens, logits,
+                        draft_probs, greedy, pad_row, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return DSPARK_ERR_INVALID_ARG;
+  if (!sizes_supported(B, K, V, r)) return DSPARK_ERR_UNSUPPORTED;
+  const WorkspaceLayout L = workspace_layout(B, K);
+  if (!workspace || workspace_bytes < L.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return DSPARK_ERR_WORKSPACE;
+
+  a.base = base_logits;
+  a.base_dtype = base_dtype;
+  a.U = U;
+  a.Wb = Wb;
+  a.w_dtype = w_dtype;
+  a.d0 = d0;
+  a.seed = seed;
+  a.offset = offset;
+  a.T = T;
+  a.greedy = greedy;
+  a.pad_row = pad_row;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.r = r;
+  a.tokens = tokens;
+  a.logits = logits;
+  a.probs = draft_probs;
+  char* ws = static_cast<char*>(workspace);
+  a.stats = reinterpret_cast<ChunkStat*>(ws + L.stats);
+  a.rowstats = reinterpret_cast<float*>(ws + L.rowstats);
+  a.control = reinterpret_cast<int*>(ws + L.control);
+
+  return DSPARK_OK;
+}
+
+// Event pairs around each kernel class: [0] position kernels, [1] picks,
+// [2] proposal writer.  Accumulated milliseconds are returned.
+struct StageTimer {
+  cudaEvent_t ev[2 * (DSPARK_MAX_K * 2 + 1)];
+  int n = 0;
+  int cls[DSPARK_MAX_K * 2 + 1];
+};
+
+dspark_status timed_launch(StageTimer* t, int cls, cudaStream_t stream,
+                           cudaError_t (*fn)(const DraftArgs&, int, int,
+                                             cudaStream_t),
+                           const DraftArgs& a, int k, int n) {
+  if (t) {
+    if (cudaEventRecord(t->ev[2 * t->n], stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  }
+  dspark_status st = from_cuda(fn(a, k, n, stream));
+  if (st != DSPARK_OK) return st;
+  if (t) {
+    if (cudaEventRecord(t->ev[2 * t->n + 1], stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    t->cls[t->n++] = cls;
+  }
+  return DSPARK_OK;
+}
+
+cudaError_t proposals_adapter(const DraftArgs& a, int, int, cudaStream_t s) {
+  return launch_proposals(a, s);
+}
+
+// The launch sequence of one draft block.
+dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
+                        StageTimer* t) {
+  const int want = sm_count() < kMaxChunks ? sm_count() : kMaxChunks;
+  const int n_chunks = generic_chunks_used(a.V, want);
+  for (int k = 0; k < a.K; ++k) {
+    dspark_status st =
+        timed_launch(t, 0, stream, launch_position_generic, a, k, want);
+    if (st != DSPARK_OK) return st;
+    st = timed_launch(t, 1, stream, launch_pick, a, k, n_chunks);
+    if (st != DSPARK_OK) return st;
+  }
+  return timed_launch(t, 2, stream, proposals_adapter, a, 0, 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dspark_version(void) { return "0.1.0"; }
+
+const char* dspark_status_string(dspark_status status) {
+  switch (status) {
+    case DSPARK_OK: return "DSPARK_OK";
+    case DSPARK_ERR_INVALID_ARG: return "DSPARK_ERR_INVALID_ARG";
+    case DSPARK_ERR_UNSUPPORTED: return "DSPARK_ERR_UNSUPPORTED";
+    case DSPARK_ERR_WORKSPACE: return "DSPARK_ERR_WORKSPACE";
+    case DSPARK_ERR_CUDA: return "DSPARK_ERR_CUDA";
+    case DSPARK_ERR_DEVICE: return "DSPARK_ERR_DEVICE";
+  }
+  return "DSPARK_UNKNOWN_STATUS";
+}
+
+size_t dspark_draft_workspace_bytes(int B, int K, int V, int r) {
+  if (!sizes_supported(B, K, V, r)) return 0;
+  return workspace_layout(B, K).total;
+}
+
+dspark_status dspark_draft_block(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream) {
+  DraftArgs a;
+  dspark_status st = prepare_draft(
+      base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
+      pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
+      workspace_bytes, a);
+  if (st != DSPARK_OK) return st;
+  return run_block(a, stream, nullptr);
+}
+
+dspark_status dspark_draft_block_profile(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, float* stage_ms, int* stage_launches,
+    cudaStream_t stream) {
+  if (!stage_ms || !stage_launches) return DSPARK_ERR_INVALID_ARG;
+  DraftArgs a;
+  dspark_status st = prepare_draft(
+      base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
+      pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
+      workspace_bytes, a);
+  if (st != DSPARK_OK) return st;
+  StageTimer t;
+  const int n_ev = 2 * (2 * K + 1);
+  int created = 0;
+  for (; created < n_ev; ++created)
+    if (cudaEventCreate(&t.ev[created]) != cudaSuccess) break;
+  if (created == n_ev) st = run_block(a, stream, &t);
+  else st = DSPARK_ERR_CUDA;
+  if (st == DSPARK_OK && cudaStreamSynchronize(stream) != cudaSuccess)
+    st = DSPARK_ERR_CUDA;
+  for (int c = 0; c < 3; ++c) {
+    stage_ms[c] = 0.0f;
+    stage_launches[c] = 0;
+  }
+  for (int i = 0; st == DSPARK_OK && i < t.n; ++i) {
+    float ms = 0.0f;
+    if (cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]) != cudaSuccess)
+      st = DSPARK_ERR_CUDA;
+    stage_ms[t.cls[i]] += ms;
+    stage_launches[t.cls[i]] += 1;
+  }
+  for (int i = 0; i < created; ++i) cudaEventDestroy(t.ev[i]);
+  return st;
+}
+
+dspark_status dspark_verify_standard(const float* draft_probs,
+                                     const float* target_probs,
+                                     const int32_t* tokens,
+                                     const uint64_t* seed,
+                                     const uint64_t* offset, int B, int K,
+                                     int V, int32_t* accepted_len,
+                                     int32_t* emitted_token,
+                                     cudaStream_t stream) {
+  if (B <= 0 || K <= 0 || V <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (!draft_probs || !target_probs || !tokens || !seed || !offset ||
+      !accepted_len || !emitted_token)
+    return DSPARK_ERR_INVALID_ARG;
+  const void* ptrs[] = {draft_probs, target_probs, tokens, seed,
+                        offset, accepted_len, emitted_token};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return DSPARK_ERR_INVALID_ARG;
+  if (B > 65535 || K > DSPARK_MAX_K || V > DSPARK_MAX_V)
+    return DSPARK_ERR_UNSUPPORTED;
+  return from_cuda(launch_verify(draft_probs, target_probs, tokens, seed,
+                                 offset, B, K, V, accepted_len, emitted_token,
+                                 stream));
+}
+
+dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,
+                                 int stream_id, int n, uint32_t* out,
+                                 float* gumbel, cudaStream_t stream) {
+  if (n <= 0 || !out || k < 0 || k > 0xffff || stream_id < 0 ||
+      stream_id > 0xffff)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!aligned16(out) || (gumbel && !aligned16(gumbel)))
+    return DSPARK_ERR_INVALID_ARG;
+  return from_cuda(
+      launch_noise_words(seed, offset, k, stream_id, n, out, gumbel, stream));
+}
+
+dspark_status dspark_read_device_error(void* workspace, int* code,
+                                       cudaStream_t stream) {
+  if (!workspace || !code) return DSPARK_ERR_INVALID_ARG;
+  // the error word is the first int of the control block at offset 0
+  int host = 0;
+  cudaError_t e = cudaMemcpyAsync(&host, workspace, sizeof(int),
+                                  cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return DSPARK_ERR_CUDA;
+  *code = host;
+  if (host == 0) return DSPARK_OK;
+  e = cudaMemsetAsync(workspace, 0, sizeof(int), stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  return e == cudaSuccess ? DSPARK_ERR_DEVICE : DSPARK_ERR_CUDA;
+}
+
+}  // extern "C"

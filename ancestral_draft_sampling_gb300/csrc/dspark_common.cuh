@@ -1,0 +1,235 @@
+// dspark_common.cuh -- device helpers shared by the sampler's kernels:
+// counter-based noise, the Gumbel transform, and the merge rules of the
+// per-chunk softmax statistics.
+//
+// Method: brb-nv/TensorRT-LLM PR #27, "2. One fused kernel per draft
+// position" (Gumbel-max with a counter-based Philox stream keyed by the
+// request's (seed, offset) draft slot of position k; per-chunk softmax
+// statistics; a small kernel picks the token).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "../../include/dspark.h"
+
+namespace dspark {
+
+// ---------------------------------------------------------------- limits
+constexpr int kMaxChunks = 1024;       // vocab chunks per position (grid.x)
+constexpr int kNoIndex = 0x7fffffff;   // "no non-NaN candidate yet"
+constexpr int kNoiseDraft = 0;         // counter stream ids
+constexpr int kNoiseAccept = 1;
+constexpr int kNoiseResample = 2;
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2,
+// 3", SC'11): ten rounds of two 32x32->64 multiplies with the published
+// multipliers, the key advanced by the published Weyl constants between
+// rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 ctr, uint2 key) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    if (round > 0) {
+      key.x += 0x9E3779B9u;
+      key.y += 0xBB67AE85u;
+    }
+    const uint32_t lo_a = 0xD2511F53u * ctr.x;
+    const uint32_t hi_a = __umulhi(0xD2511F53u, ctr.x);
+    const uint32_t lo_b = 0xCD9E8D57u * ctr.z;
+    const uint32_t hi_b = __umulhi(0xCD9E8D57u, ctr.z);
+    ctr = make_uint4(hi_b ^ ctr.y ^ key.x, lo_b, hi_a ^ ctr.w ^ key.y, lo_a);
+  }
+  return ctr;
+}
+
+// The Philox block that holds the words of elements 4*blk .. 4*blk+3 of
+// stream `stream` at position k for request (seed, offset).
+__device__ __forceinline__ uint4 noise_block(uint64_t seed, uint64_t offset,
+                                             int k, int stream, uint32_t blk) {
+  const uint4 ctr = make_uint4(blk, (uint32_t)k | ((uint32_t)stream << 16),
+                               (uint32_t)offset, (uint32_t)(offset >> 32));
+  const uint2 key = make_uint2((uint32_t)seed, (uint32_t)(seed >> 32));
+  return philox4x32_10(ctr, key);
+}
+
+__device__ __forceinline__ uint32_t word_of(uint4 w, int i) {
+  return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
+}
+
+// Standard Gumbel variate g = -log(-log(1 - w)), w = (x + 0.5) * 2^-32, in
+// float32.  The exponential variate E = -log(1 - w) is formed from whichever
+// of w and 1 - w is at most one half, so that both tails keep full relative
+// precision: E = -log1p(-w) when w <= 1/2, and E = -log(1 - w) with
+// 1 - w = (~x + 0.5) * 2^-32 otherwise.  Both forms are exact rewrites of
+// the same quantity; only their rounding differs.
+__device__ __forceinline__ float gumbel_from_word(uint32_t x) {
+  float e;
+  if (x < 0x80000000u) {
+    const float w = fmaf((float)x, 0x1p-32f, 0x1p-33f);
+    e = -log1pf(-w);
+  } else {
+    const float one_minus_w = fmaf((float)(~x), 0x1p-32f, 0x1p-33f);
+    e = -logf(one_minus_w);
+  }
+  return -logf(e);
+}
+
+// Uniform in (0, 1) for the acceptance test, exact in float32:
+// ((x >> 9) + 0.5) * 2^-23.
+__device__ __forceinline__ float accept_uniform(uint32_t x) {
+  return ((float)(x >> 9) + 0.5f) * 0x1p-23f;
+}
+
+// ------------------------------------------------- chunk softmax statistics
+// Per (request, vocab chunk): the best decision score and its index, and the
+// running (max m, sum exp(s - m)) of the scaled logits.
+struct alignas(16) ChunkStat {
+  float best;  // largest non-NaN decision score (s + g, or s for greedy)
+  int idx;     // its lowest index; kNoIndex if every score was NaN
+  float m;     // max of the non-NaN scaled logits (-inf if none)
+  float s;     // sum of exp(s_v - m) (NaN if any s_v was NaN)
+};
+
+// Candidate order: larger score first, then the lower index; an entry with
+// idx == kNoIndex (nothing but NaN seen) loses to anything.
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+  if (ib == kNoIndex) return true;
+  if (ia == kNoIndex) return false;
+  if (sa != sb) return sa > sb;
+  return ia < ib;
+}
+
+__device__ __forceinline__ void merge_argmax(float& best, int& idx, float ob,
+                                             int oi) {
+  if (!better(best, idx, ob, oi)) {
+    best = ob;
+    idx = oi;
+  }
+}
+
+// (m, s) (+) (om, os): the sum-exp of the union, relative to the larger max.
+__device__ __forceinline__ void merge_sumexp(float& m, float& s, float om,
+                                             float os) {
+  const float mn = fmaxf(m, om);
+  if (mn == -INFINITY) {
+    s = __fadd_rn(s, os);  // both empty (0) or carrying a NaN
+  } else {
+    // explicit roundings: no FMA contraction, so (a, b) and (b, a) agree
+    s = __fadd_rn(__fmul_rn(s, expf(m - mn)), __fmul_rn(os, expf(om - mn)));
+  }
+  m = mn;
+}
+
+__device__ __forceinline__ void merge_stat(ChunkStat& a, const ChunkStat& b) {
+  merge_argmax(a.best, a.idx, b.best, b.idx);
+  merge_sumexp(a.m, a.s, b.m, b.s);
+}
+
+__device__ __forceinline__ ChunkStat shfl_xor_stat(const ChunkStat& a,
+                                                   int lane_mask) {
+  ChunkStat o;
+  o.best = __shfl_xor_sync(0xffffffffu, a.best, lane_mask);
+  o.idx = __shfl_xor_sync(0xffffffffu, a.idx, lane_mask);
+  o.m = __shfl_xor_sync(0xffffffffu, a.m, lane_mask);
+  o.s = __shfl_xor_sync(0xffffffffu, a.s, lane_mask);
+  return o;
+}
+
+// Butterfly reduction over the 32 lanes; every lane ends with the result.
+// merge_stat(a, b) and merge_stat(b, a) give the same bits (max, the index
+// tie-break and the two-term IEEE sum are all commutative), so partners
+// agree and the result is bitwise reproducible.
+__device__ __forceinline__ ChunkStat warp_reduce_stat(ChunkStat a) {
+#pragma unroll
+  for (int mask = 16; mask > 0; mask >>= 1) {
+    const ChunkStat o = shfl_xor_stat(a, mask);
+    merge_stat(a, o);
+  }
+  return a;
+}
+
+__device__ __forceinline__ ChunkStat empty_stat() {
+  ChunkStat e;
+  e.best = -INFINITY;
+  e.idx = kNoIndex;
+  e.m = -INFINITY;
+  e.s = 0.0f;
+  return e;
+}
+
+// --------------------------------------------------------------- bf16 load
+__device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
+  return __uint_as_float((uint32_t)b << 16);
+}
+
+// ------------------------------------------------------- workspace layout
+struct WorkspaceLayout {
+  size_t control;   // 256 B at offset 0: device error word and counters
+  size_t stats;     // [B, kMaxChunks] ChunkStat
+  size_t rowstats;  // [B, K, 2] float (M, S)
+  size_t total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) {
+  return (x + a - 1) / a * a;
+}
+
+__host__ __device__ inline WorkspaceLayout workspace_layout(int B, int K) {
+  WorkspaceLayout L;
+  size_t off = 0;
+  L.control = off;
+  off += 256;
+  L.stats = off;
+  off = align_up(off + (size_t)B * kMaxChunks * sizeof(ChunkStat), 256);
+  L.rowstats = off;
+  off = align_up(off + (size_t)B * K * 2 * sizeof(float), 256);
+  L.total = off;
+  return L;
+}
+
+// Device error codes written to the control word.
+enum DeviceError : int {
+  kDevErrNone = 0,
+  kDevErrBadToken = 1,  // a d0 entry outside [0, V) (token 0 used instead)
+};
+
+// ------------------------------------------------------- kernel launchers
+struct DraftArgs {
+  const void* base;
+  int base_dtype;
+  const void* U;
+  const void* Wb;
+  int w_dtype;
+  const int32_t* d0;
+  const uint64_t* seed;
+  const uint64_t* offset;
+  float T;
+  const uint8_t* greedy;
+  const uint8_t* pad_row;
+  int B, K, V, r;
+  int32_t* tokens;
+  float* logits;
+  float* probs;
+  ChunkStat* stats;
+  float* rowstats;
+  int* control;
+};
+
+// Launch helpers (each returns the cudaGetLastError of its launch).
+cudaError_t launch_position_generic(const DraftArgs& a, int k, int n_chunks,
+                                    cudaStream_t stream);
+cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
+                        cudaStream_t stream);
+cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream);
+cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
+                          const uint64_t* seed, const uint64_t* offset, int B,
+                          int K, int V, int32_t* accepted_len,
+                          int32_t* emitted, cudaStream_t stream);
+cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
+                               int stream_id, int n, uint32_t* out,
+                               float* gumbel, cudaStream_t stream);
+
+}  // namespace dspark

@@ -1,0 +1,131 @@
+// pick_propose.cu -- the cross-chunk pick and the post-block proposal writer.
+//
+// brb-nv/TensorRT-LLM PR #27, "2. One fused kernel per draft position":
+// "a small kernel picks the token" from the per-chunk statistics, and after
+// the block one kernel writes q_k = softmax(logits_k / T) for every position
+// from the float32 biased logits, recomputing logits_k / T bit for bit as the
+// draw used it.  Greedy requests store a one-hot proposal (PR #27, Test
+// Coverage, "Also checked").
+#include "dspark_common.cuh"
+
+namespace dspark {
+namespace {
+
+constexpr int kPickThreads = 256;
+
+// One CTA per request: merge the chunk statistics of position k in a fixed
+// order, write d_k and the row's (M, S).
+__global__ void __launch_bounds__(kPickThreads)
+pick_kernel(DraftArgs a, int k, int n_chunks) {
+  __shared__ ChunkStat part[kPickThreads / 32];
+  const int b = blockIdx.x;
+  ChunkStat st = empty_stat();
+  for (int c = threadIdx.x; c < n_chunks; c += kPickThreads)
+    merge_stat(st, a.stats[(size_t)b * kMaxChunks + c]);
+  st = warp_reduce_stat(st);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) part[warp] = st;
+  __syncthreads();
+  if (warp == 0) {
+    st = lane < kPickThreads / 32 ? part[lane] : empty_stat();
+    st = warp_reduce_stat(st);
+    if (lane == 0) {
+      const size_t row = (size_t)b * a.K + k;
+      a.tokens[row] = (st.idx == kNoIndex) ? 0 : st.idx;
+      a.rowstats[2 * row] = st.m;
+      a.rowstats[2 * row + 1] = st.s;
+    }
+  }
+}
+
+constexpr int kPropThreads = 256;
+constexpr int kPropPerThread = 8;  // two float4 per thread per row segment
+
+__device__ __forceinline__ float scale(float l, float T) {
+  return T == 1.0f ? l : __fdiv_rn(l, T);
+}
+
+// grid = (B*K rows, segments of a row).  q = exp(s - M) * (1 / S).
+template <bool kVec>
+__global__ void __launch_bounds__(kPropThreads)
+proposals_kernel(DraftArgs a) {
+  const int row = blockIdx.x;
+  const int b = row / a.K;
+  const int V = a.V;
+  const float M = a.rowstats[2 * (size_t)row];
+  const float invS = __frcp_rn(a.rowstats[2 * (size_t)row + 1]);
+  const bool greedy = a.greedy != nullptr && a.greedy[b] != 0;
+  const int token = greedy ? a.tokens[row] : -1;
+  const float* lrow = a.logits + (size_t)row * V;
+  float* qrow = a.probs + (size_t)row * V;
+  const float T = a.T;
+  const int seg = kPropThreads * kPropPerThread;
+  const int v_begin = blockIdx.y * seg;
+  if (kVec) {
+#pragma unroll
+    for (int i = 0; i < kPropPerThread / 4; ++i) {
+      const int v = v_begin + (i * kPropThreads + threadIdx.x) * 4;
+      if (v >= V) break;  // V % 4 == 0: the whole float4 is in range
+      const float4 l = __ldcs(reinterpret_cast<const float4*>(lrow + v));
+      float4 q;
+      if (greedy) {
+        q = make_float4(v == token, v + 1 == token, v + 2 == token, v + 3 == token);
+      } else {
+        q.x = __fmul_rn(expf(scale(l.x, T) - M), invS);
+        q.y = __fmul_rn(expf(scale(l.y, T) - M), invS);
+        q.z = __fmul_rn(expf(scale(l.z, T) - M), invS);
+        q.w = __fmul_rn(expf(scale(l.w, T) - M), invS);
+      }
+      __stcs(reinterpret_cast<float4*>(qrow + v), q);
+    }
+  } else {
+    for (int i = 0; i < kPropPerThread; ++i) {
+      const int v = v_begin + i * kPropThreads + threadIdx.x;
+      if (v >= V) break;
+      const float q = greedy ? (v == token ? 1.0f : 0.0f)
+                             : __fmul_rn(expf(scale(lrow[v], T) - M), invS);
+      qrow[v] = q;
+    }
+  }
+}
+
+constexpr int kNoiseThreads = 256;
+
+__global__ void noise_words_kernel(uint64_t seed, uint64_t offset, int k,
+                                   int stream_id, int n, uint32_t* out,
+                                   float* gumbel) {
+  const int v = blockIdx.x * kNoiseThreads + threadIdx.x;
+  if (v >= n) return;
+  const uint4 w = noise_block(seed, offset, k, stream_id, (uint32_t)v >> 2);
+  const uint32_t x = word_of(w, v & 3);
+  out[v] = x;
+  if (gumbel) gumbel[v] = gumbel_from_word(x);
+}
+
+}  // namespace
+
+cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
+                        cudaStream_t stream) {
+  pick_kernel<<<a.B, kPickThreads, 0, stream>>>(a, k, n_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream) {
+  const int seg = kPropThreads * kPropPerThread;
+  const dim3 grid(a.B * a.K, (a.V + seg - 1) / seg);
+  if (a.V % 4 == 0)
+    proposals_kernel<true><<<grid, kPropThreads, 0, stream>>>(a);
+  else
+    proposals_kernel<false><<<grid, kPropThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
+                               int stream_id, int n, uint32_t* out,
+                               float* gumbel, cudaStream_t stream) {
+  noise_words_kernel<<<(n + kNoiseThreads - 1) / kNoiseThreads, kNoiseThreads,
+                       0, stream>>>(seed, offset, k, stream_id, n, out, gumbel);
+  return cudaGetLastError();
+}
+
+}  // namespace dspark

@@ -1,0 +1,418 @@
+"""Benchmark of the DSpark ancestral draft-block sampler on one GB300.
+
+One step = one whole K=7 draft block (every position kernel, pick and the
+proposal writer) over the B=88, V=200064, r=256 workload (float32 drafter
+logits, bfloat16 Markov head, T=1, requests 80..87 are CUDA-graph padding
+rows), replayed from a CUDA graph -- the configuration the throughput target
+is stated on.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (test infrastructure) on the host cores
+on a bounded sample of the same workload.  Under torchrun (N > 1) every rank
+runs an independent replica (no collective on the path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs per K=7 draft block (B×7×200064, r=256) and achieved HBM GB/s vs peak"
+PAGES_US_B88 = 841.0  # PR #27 Results, "Drafting alone", B=88 (GB300)
+CONFIG_ID = 4
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def workload_desc(w):
+    return {
+        "workload": ("draft block B=88 K=7 V=200064 r=256: f32 drafter logits "
+                     "N(0,4^2)+32 spikes/row, bf16 U,Wb N(0,0.02^2), T=1, "
+                     "requests 80-87 CUDA-graph padding rows (NaN logits)"),
+        "B": w.B, "K": w.K, "V": w.V, "r": w.r,
+        "base_dtype": "f32" if w.base_dtype == 0 else "bf16",
+        "head_dtype": "bf16" if w.w_dtype == 1 else "f32",
+        "timing": "CUDA-graph replay of dspark_draft_block, CUDA events",
+        "l2": "inputs larger than L2 (2.7 GB touched per step; base 493 MB)",
+    }
+
+
+def compulsory_bytes(w):
+    """Algorithmic bytes of one block: base read once, Wb read once per
+    position, logits written, logits re-read by the proposal writer,
+    proposals written (gathers, statistics and tokens are below 0.1%)."""
+    elt = 4 if w.base_dtype == 0 else 2
+    welt = 2 if w.w_dtype == 1 else 4
+    B, K, V, r = w.B, w.K, w.V, w.r
+    return B * K * V * elt + K * r * V * welt + 3 * B * K * V * 4
+
+
+def position_kernel_bytes(w):
+    """Algorithmic bytes of one position-kernel launch: base_k read, Wb read,
+    logits_k written, the B gathered U rows read."""
+    elt = 4 if w.base_dtype == 0 else 2
+    welt = 2 if w.w_dtype == 1 else 4
+    return w.B * w.V * elt + w.r * w.V * welt + w.B * w.V * 4 + w.B * w.r * welt
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self._t.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows
+                          for i, f in enumerate(flags) if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(rows)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ancestral_draft_sampling_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, or
+    None when the kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = d.get(kernel)
+    if not ent or ent.get("source_hash") != kernel_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ CPU oracle
+def oracle_block_seconds(w, n_requests: int, threads: int):
+    """Wall seconds for the oracle to draft `n_requests` requests (all K
+    positions each, in order) with `threads` host threads."""
+    import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    def one(b):
+        prev = int(w.d0[b])
+        pad = bool(w.pad_row[b]) if w.pad_row is not None else False
+        greedy = bool(w.greedy[b]) if w.greedy is not None else False
+        for k in range(w.K):
+            res = oracle.draft_position(None if pad else w.base[b, k], w.U, w.Wb,
+                                        prev, int(w.seed[b]), int(w.offset[b]),
+                                        k, w.T, greedy=greedy, is_pad=pad)
+            prev = res.token
+        return prev
+
+    reqs = list(range(n_requests))
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(one, reqs))
+    return time.perf_counter() - t0
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, budget_s: float = 20.0):
+    threads = cpu_threads()
+    n = min(w.B, threads)
+    t = oracle_block_seconds(w, n, threads)
+    waves_full = -(-w.B // threads)
+    per_block_s = t * waves_full  # one wave of n <= threads requests took t
+    return {
+        "value": per_block_s * 1e6, "unit": "us", "cores": threads,
+        "kind": "oracle",
+        "sample": (f"{n} of {w.B} requests x {w.K} positions in one parallel "
+                   f"wave ({t:.2f} s), scaled by {waves_full} waves to a full "
+                   f"block"),
+    }
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    from ancestral_draft_sampling_gb300 import workloads as wl
+    w = wl.make_config(CONFIG_ID)
+    threads = cpu_threads()
+    n = min(w.B, threads)
+    for _ in range(args.warmup):
+        oracle_block_seconds(w, n, threads)
+    times = [oracle_block_seconds(w, n, threads) for _ in range(args.steps)]
+    waves = -(-w.B // threads)
+    us = statistics.mean(times) * waves * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": "us",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_desc(w),
+        "cpu_baseline": {"value": us, "unit": "us", "cores": threads,
+                         "kind": "oracle",
+                         "sample": (f"each step: {n} of {w.B} requests x {w.K} "
+                                    f"positions in one parallel wave, scaled "
+                                    f"by {waves} waves")},
+        "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------- GPU arm
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build_library()
+    import ancestral_draft_sampling_gb300 as pkg
+    from ancestral_draft_sampling_gb300 import workloads as wl
+    from tests.parity import to_device
+
+    local = _env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    w = wl.make_config(CONFIG_ID)
+    dev = to_device(w, f"cuda:{local}")
+    B, K, V, r = w.B, w.K, w.V, w.r
+    tokens = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    logits = torch.empty((B, K, V), dtype=torch.float32, device="cuda")
+    probs = torch.empty((B, K, V), dtype=torch.float32, device="cuda")
+    ws = pkg.DraftWorkspace(B, K, V, r)
+
+    def call(stream=None):
+        pkg.draft_block(dev["base"], dev["U"], dev["Wb"], dev["d0"], dev["seed"],
+                        dev["offset"], w.T, greedy=dev["greedy"],
+                        pad_row=dev["pad_row"], tokens=tokens, logits=logits,
+                        draft_probs=probs, workspace=ws, stream=stream)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        call(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        call(side)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    cur = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        torch.cuda.synchronize()
+        ev0.record(cur)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(cur)
+        torch.cuda.synchronize()
+    ms_total = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([ms_total], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+    ms_step = ms_total / args.steps
+    us_per_block = ms_step * 1e3 / world  # whole job: N replicas in parallel
+
+    # per-kernel durations, CUDA events around every launch on its stream
+    prof = {"position": [0.0, 0], "pick": [0.0, 0], "proposal": [0.0, 0]}
+    for _ in range(max(3, min(args.steps, 10))):
+        p = pkg.draft_block_profile(dev["base"], dev["U"], dev["Wb"], dev["d0"],
+                                    dev["seed"], dev["offset"], w.T,
+                                    greedy=dev["greedy"], pad_row=dev["pad_row"],
+                                    tokens=tokens, logits=logits,
+                                    draft_probs=probs, workspace=ws)
+        for key, (ms, n) in p.items():
+            prof[key][0] += ms
+            prof[key][1] += n
+    dominant = max(prof, key=lambda k: prof[k][0])
+    avg_ms = {k: (v[0] / v[1] if v[1] else 0.0) for k, v in prof.items()}
+    peak, peak_kind = measured_peaks()
+    if dominant == "position":
+        alg_bytes = position_kernel_bytes(w)
+    elif dominant == "proposal":
+        alg_bytes = 2 * B * K * V * 4
+    else:
+        alg_bytes = B * 1024 * 16
+    achieved = alg_bytes / (avg_ms[dominant] * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved,
+                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": achieved / peak,
+                "traffic": ncu_traffic(dominant),
+                "alg_bytes_per_launch": alg_bytes,
+                "avg_launch_ms": avg_ms[dominant],
+                "stage_avg_ms": avg_ms,
+                "stage_share": {k: v[0] / sum(x[0] for x in prof.values())
+                                for k, v in prof.items()}}
+    block_gbs = compulsory_bytes(w) / (ms_step * 1e-3) / 1e9
+
+    # end to end through the public API with host buffers
+    host_base = torch.from_numpy(
+        w.base if w.base.dtype == np.float32 else w.base.view(np.int16)).pin_memory()
+    if w.base.dtype != np.float32:
+        host_base = host_base.view(torch.bfloat16)
+    host_small = {k: dev[k].cpu().pin_memory() for k in ("d0", "seed", "offset")}
+    host_tokens = torch.empty((B, K), dtype=torch.int32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 10))
+    cur = torch.cuda.current_stream()
+
+    def e2e_step():
+        dev["base"].copy_(host_base, non_blocking=True)
+        for k2, t in host_small.items():
+            dev[k2].copy_(t, non_blocking=True)
+        call()
+        host_tokens.copy_(tokens, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cur)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) / e2e_steps * 1e3 / world
+    h2d = host_base.numel() * host_base.element_size() + sum(
+        t.numel() * t.element_size() for t in host_small.values())
+    d2h = host_tokens.numel() * 4
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": us_per_block, "unit": "us",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_step, "higher_is_better": False,
+            "scaling": "weak",
+            "vs_baseline": us_per_block / PAGES_US_B88,
+            "dtype": "f32", "data": "synthetic",
+            "config": dict(workload_desc(w), parallelism=f"replicas x{world}"),
+            "block_hbm_gbs": block_gbs,
+            "block_hbm_frac": block_gbs / peak,
+            "compulsory_bytes_per_block": compulsory_bytes(w),
+            "roofline": roofline,
+            "clocks": clocks.summary(),
+            "gpu_launches": args.steps * (2 * K + 1),
+            "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h,
+                    "path": "pinned host -> device copies, dspark_draft_block, "
+                            "tokens device -> pinned host"},
+        }
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(w)
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank = _env_int("RANK", 0)
+    world = _env_int("WORLD_SIZE", args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_ours(args, rank, world)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

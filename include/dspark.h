@@ -1,0 +1,206 @@
+/*
+ * dspark.h -- C ABI of the GB300 (sm_103a) DSpark ancestral draft-block
+ * sampler.
+ *
+ * The method (brb-nv/TensorRT-LLM PR #21, "2. Golden sampling semantics";
+ * brb-nv/TensorRT-LLM PR #27, "2. One fused kernel per draft position"):
+ * for request b and draft position k = 0..K-1,
+ *     l_k   = base_k + bias(d_{k-1}),   bias(d) = U[d] @ Wb   (rank-r head)
+ *     s_k   = l_k / T                   (float32 IEEE division)
+ *     d_k   = argmax_v (s_k[v] + g[v])  (Gumbel-max; g from Philox noise
+ *                                        keyed by (seed, offset, k))
+ *     q_k   = softmax(s_k)              (the proposal, written after the
+ *                                        block from the same float32 l_k)
+ * with d_{-1} = d0[b], the last accepted token.  Greedy requests take
+ * d_k = argmax_v s_k[v] and store a one-hot proposal.  CUDA-graph padding
+ * rows draw from the bias alone.  Verification is standard token-level
+ * rejection sampling (PR #21, "2. Golden sampling semantics").
+ *
+ * Noise (reading of PR #27, "2. One fused kernel per draft position"):
+ * Philox4x32-10 with key = (seed lo, seed hi) and counter
+ * (v >> 2, k | stream << 16, offset lo, offset hi), word v & 3; stream 0
+ * feeds the draft, 1 the acceptance uniforms, 2 the residual / bonus draws.
+ * g = -log(-log1p(-w)), w = (x + 0.5) * 2^-32.  Ties go to the lowest index;
+ * a NaN score never wins (a row whose scores are all NaN yields token 0).
+ *
+ * Conventions for every entry point:
+ *   - All tensors are dense, row-major, and live in device memory unless
+ *     stated otherwise.  The caller owns every buffer; the library does not
+ *     allocate, free, synchronise, print or trap.
+ *   - Calls are asynchronous on `stream` and may be captured in a CUDA graph
+ *     (all launches are plain kernel launches on `stream`).
+ *   - Argument checks run on the host before any launch; a failing check
+ *     returns a status and enqueues nothing.  A launch failure returns
+ *     DSPARK_ERR_CUDA (from cudaGetLastError).
+ *   - Results are bitwise deterministic given the inputs on a given GPU
+ *     model (fixed reduction order, counter-based noise).
+ */
+#ifndef DSPARK_H_
+#define DSPARK_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define DSPARK_API __attribute__((visibility("default")))
+#else
+#define DSPARK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { DSPARK_F32 = 0, DSPARK_BF16 = 1 } dspark_dtype;
+
+typedef enum {
+  DSPARK_OK = 0,
+  DSPARK_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, bad T,
+                                 misaligned pointer, out-of-range token */
+  DSPARK_ERR_UNSUPPORTED = 2, /* valid but outside the supported shapes */
+  DSPARK_ERR_WORKSPACE = 3,   /* workspace missing or too small */
+  DSPARK_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed */
+  DSPARK_ERR_DEVICE = 5       /* a kernel recorded an error in the workspace
+                                 (a bounded wait ran out); see
+                                 dspark_read_device_error */
+} dspark_status;
+
+/* Supported shapes: 1 <= B <= 1024, 1 <= K <= 64, 1 <= V <= 2^26,
+ * 16 <= r <= 256 with r % 16 == 0.  (PR #27, Results: B x 7 x 200064
+ * logits and a rank-256 head sit inside these limits.) */
+#define DSPARK_MAX_B 1024
+#define DSPARK_MAX_K 64
+#define DSPARK_MAX_R 256
+#define DSPARK_MAX_V (1 << 26)
+
+/*
+ * Bytes of device workspace dspark_draft_block needs for these sizes
+ * (0 if the sizes are unsupported).  The workspace holds per-chunk softmax
+ * statistics, per-row (max, sum-exp) of every position, and a device error
+ * word.  Its contents need not be initialised and are overwritten by each
+ * call; two calls in flight at the same time must not share a workspace.
+ */
+DSPARK_API size_t dspark_draft_workspace_bytes(int B, int K, int V, int r);
+
+/*
+ * dspark_draft_block -- ancestral drafting of one K-token block for B
+ * requests (PR #27, "2. One fused kernel per draft position").
+ *
+ *   base_logits  [B,K,V] base_dtype (F32 or BF16); read only, never modified
+ *                (PR #27, Test Coverage: the drafter's logits are left as
+ *                they are).  Rows of padding requests may hold anything,
+ *                NaN included.
+ *   U            [V,r] w_dtype;  Wb [r,V] w_dtype (F32 or BF16, both the
+ *                same dtype).  bias(d) = U[d] @ Wb, accumulated in float32.
+ *   d0           [B] int32, the last accepted token of each request, in
+ *                [0, V).  An entry outside that range is replaced by 0 and
+ *                the workspace's device error word is set to 1 (read it with
+ *                dspark_read_device_error).
+ *   seed, offset [B] uint64 each: the request's noise key and draft slot.
+ *                A new offset draws anew (PR #27, Test Coverage).
+ *   T            temperature, finite and > 0 (the same for every request).
+ *   greedy       [B] uint8 or NULL: nonzero = greedy request (argmax chain,
+ *                one-hot proposal, no noise consumed).  NULL = all sampled.
+ *   pad_row      [B] uint8 or NULL: nonzero = CUDA-graph padding row; its
+ *                base logits are ignored and l = bias (PR #27: padding rows
+ *                draw from the bias alone).
+ *   tokens       [B,K] int32 out: the drafted tokens d_k.
+ *   logits       [B,K,V] float32 out: the biased logits l_k.
+ *   draft_probs  [B,K,V] float32 out: the proposals q_k.
+ *   workspace    device scratch of at least
+ *                dspark_draft_workspace_bytes(B,K,V,r) bytes, 256-byte
+ *                aligned.
+ * Alignment: every device pointer must be at least 16-byte aligned
+ * (DSPARK_ERR_INVALID_ARG otherwise).
+ */
+DSPARK_API dspark_status dspark_draft_block(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * dspark_draft_block_profile -- measurement variant of dspark_draft_block:
+ * the same argument checks and the same launch sequence, with a pair of CUDA
+ * events recorded on `stream` around every launch.  It then synchronises
+ * `stream` and returns, per kernel class, the summed event time and the
+ * number of launches:
+ *   stage_ms[3], stage_launches[3]  (host arrays) -- [0] the K position
+ *   kernels, [1] the K pick kernels, [2] the proposal writer.
+ * Outputs are identical to dspark_draft_block's.  Because it synchronises
+ * and creates events, it must not be captured in a CUDA graph.
+ */
+DSPARK_API dspark_status dspark_draft_block_profile(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, float* stage_ms, int* stage_launches,
+    cudaStream_t stream);
+
+/*
+ * dspark_verify_standard -- standard token-level rejection sampling of the
+ * drafts (PR #21, "2. Golden sampling semantics": the default rule), for B
+ * requests.
+ *
+ *   draft_probs  [B,K,V] float32: the proposals q_k the drafts came from.
+ *   target_probs [B,K+1,V] float32: the target's p_k for the drafted prefix;
+ *                row K is the bonus distribution.
+ *   tokens       [B,K] int32 drafts, each in [0, V) (a token outside it makes
+ *                that request report accepted_len = -1).
+ *   seed, offset [B] uint64 (streams 1 and 2 of the counter layout above).
+ *   accepted_len [B] int32 out: number of accepted drafts, 0..K.
+ *   emitted_token[B] int32 out: the token emitted after the accepted prefix
+ *                (the residual draw at the first rejection, or the bonus
+ *                draw from p_K when all K are accepted).
+ * Draft k is accepted iff float(u_k * q_k[d_k]) < p_k[d_k] with
+ * u_k = ((x >> 9) + 0.5) * 2^-23 from stream 1 word 0 at position k.  The
+ * residual is max(p_k - q_k, 0) (p_k itself if that is all zero); draws are
+ * Gumbel-max over log(weight) with stream 2 noise at the drawing position.
+ */
+DSPARK_API dspark_status dspark_verify_standard(const float* draft_probs,
+                                     const float* target_probs,
+                                     const int32_t* tokens,
+                                     const uint64_t* seed,
+                                     const uint64_t* offset, int B, int K,
+                                     int V, int32_t* accepted_len,
+                                     int32_t* emitted_token,
+                                     cudaStream_t stream);
+
+/*
+ * dspark_noise_words -- diagnostic: writes the n raw Philox words the
+ * sampler uses for elements 0..n-1 of (seed, offset, position k, stream),
+ * i.e. out[v] = word (v & 3) of Philox4x32-10(counter (v >> 2,
+ * k | stream << 16, offset lo, offset hi), key (seed lo, seed hi)), and
+ * gumbel[v] = the float32 Gumbel variate the draft kernel derives from it
+ * (gumbel may be NULL).  out/gumbel are device pointers.
+ */
+DSPARK_API dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,
+                                 int stream_id, int n, uint32_t* out,
+                                 float* gumbel, cudaStream_t stream);
+
+/*
+ * dspark_read_device_error -- copies the device error word of `workspace`
+ * to the host (synchronising `stream`) and clears it.  Returns DSPARK_OK if
+ * no kernel recorded an error, DSPARK_ERR_DEVICE (and *code != 0) if one
+ * did.  This is the only call that synchronises.
+ */
+DSPARK_API dspark_status dspark_read_device_error(void* workspace, int* code,
+                                       cudaStream_t stream);
+
+/* Human-readable name of a status. */
+DSPARK_API const char* dspark_status_string(dspark_status status);
+
+/* Library version, "major.minor.patch". */
+DSPARK_API const char* dspark_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSPARK_H_ */

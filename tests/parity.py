@@ -1,0 +1,125 @@
+"""Parity helpers: move a synthetic workload to the GPU, run the C-ABI path,
+and compare its outputs with the CPU oracle row by row.
+
+Tolerances (the spec bar, with one derived widening):
+  tokens       identical, except where the oracle's two best decision scores
+               lie within 1e-5 of each other (a near tie that float32 noise or
+               a one-ulp logit difference may resolve either way);
+  logits       |gpu - oracle| <= 1e-6 + 1e-5 |oracle|;
+  draft_probs  |gpu - oracle| <= 1e-6 + rtol_q |oracle| with
+               rtol_q = max(1e-5, 4 ulp(max |s|)), s = l / T.  The kernels
+               accumulate the bias in float32 while the oracle rounds a double
+               once, so l may differ by one ulp; exp(s - M) then moves by
+               ulp(l) / T relative, which for T >= 0.7 and |l| < 32 stays
+               below 1e-5 and for small T (e.g. 0.05) needs the 4-ulp term.
+Comparisons are teacher-forced: position k of request b is recomputed by the
+oracle from the token the GPU drew at k-1, so one allowed near-tie
+divergence does not shift the rest of the row.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TOKEN_TIE = 1e-5
+LOGIT_ATOL, LOGIT_RTOL = 1e-6, 1e-5
+PROB_ATOL, PROB_RTOL = 1e-6, 1e-5
+
+
+def _t(a: np.ndarray, device):
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    if a.dtype == np.uint64:
+        return torch.from_numpy(a.view(np.int64)).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def to_device(w, device="cuda:0") -> dict:
+    d = {
+        "base": _t(w.base, device),
+        "U": _t(w.U, device),
+        "Wb": _t(w.Wb, device),
+        "d0": _t(w.d0.astype(np.int32), device),
+        "seed": _t(w.seed, device),
+        "offset": _t(w.offset, device),
+        "greedy": None if w.greedy is None else _t(w.greedy, device),
+        "pad_row": None if w.pad_row is None else _t(w.pad_row, device),
+    }
+    if w.target is not None:
+        d["target"] = _t(w.target, device)
+    return d
+
+
+def ulp32(x: float) -> float:
+    x = abs(float(x))
+    if x == 0 or not np.isfinite(x):
+        return 2.0**-149
+    return 2.0 ** (np.floor(np.log2(x)) - 23)
+
+
+def prob_rtol(logits_row: np.ndarray, T: float) -> float:
+    s = np.abs(logits_row[np.isfinite(logits_row)]) / T
+    smax = float(s.max()) if s.size else 0.0
+    return max(PROB_RTOL, 4 * ulp32(smax))
+
+
+def default_rows(B, K, max_rows=None, seed=0):
+    rows = [(b, k) for b in range(B) for k in range(K)]
+    if max_rows is None or len(rows) <= max_rows:
+        return rows
+    first = [(b, 0) for b in range(B)]
+    rest = [rk for rk in rows if rk[1] > 0]
+    rng = np.random.Generator(np.random.PCG64(seed))
+    pick = rng.choice(len(rest), size=max(0, max_rows - len(first)), replace=False)
+    return sorted(first + [rest[i] for i in pick])
+
+
+def check_block_against_oracle(w, tokens, logits, probs, rows=None,
+                               threads=None):
+    """Asserts parity of the GPU outputs (numpy) on `rows` (default: all).
+    Returns a dict of counters (rows checked, near-tie token differences)."""
+    B, K, V = w.B, w.K, w.V
+    rows = rows or default_rows(B, K)
+    assert tokens.shape == (B, K)
+    assert ((tokens >= 0) & (tokens < V)).all(), "token out of range"
+    prev = np.concatenate([w.d0[:, None].astype(np.int32), tokens[:, :-1]], axis=1)
+    res = oracle.draft_rows(w.base, w.U, w.Wb, prev, w.seed, w.offset, w.T,
+                            rows, greedy=w.greedy, pad_row=w.pad_row,
+                            threads=threads)
+    ties = 0
+    for (b, k), o in zip(rows, res):
+        where = f"(b={b}, k={k})"
+        if tokens[b, k] != o.token:
+            gap = o.best - o.second
+            assert gap <= TOKEN_TIE, (
+                f"token {where}: gpu {tokens[b, k]} oracle {o.token}, "
+                f"oracle top-2 gap {gap}")
+            ties += 1
+        np.testing.assert_allclose(logits[b, k], o.logits, rtol=LOGIT_RTOL,
+                                   atol=LOGIT_ATOL, equal_nan=True,
+                                   err_msg=f"logits {where}")
+        greedy = w.greedy is not None and w.greedy[b]
+        if greedy:
+            onehot = np.zeros(V, np.float32)
+            onehot[tokens[b, k]] = 1.0
+            np.testing.assert_array_equal(probs[b, k], onehot,
+                                          err_msg=f"greedy proposal {where}")
+        else:
+            np.testing.assert_allclose(
+                probs[b, k], o.probs, atol=PROB_ATOL,
+                rtol=prob_rtol(o.logits, w.T), equal_nan=True,
+                err_msg=f"draft_probs {where}")
+    return {"rows": len(rows), "near_tie_token_diffs": ties}
+
+
+def run_draft(w, dev=None, device="cuda:0", stream=None, workspace=None):
+    import ancestral_draft_sampling_gb300 as pkg
+    dev = dev or to_device(w, device)
+    out = pkg.draft_block(dev["base"], dev["U"], dev["Wb"], dev["d0"],
+                          dev["seed"], dev["offset"], w.T,
+                          greedy=dev["greedy"], pad_row=dev["pad_row"],
+                          workspace=workspace, stream=stream)
+    torch.cuda.synchronize()
+    return out

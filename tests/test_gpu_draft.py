@@ -1,0 +1,237 @@
+"""GPU parity of the draft-block path (through the C ABI) against the CPU
+oracle, plus the properties the pages test: conditioning, chi-square of the
+draws, graph replay == eager, new offset draws anew, padding rows, greedy
+rows, untouched drafter logits."""
+import numpy as np
+import pytest
+import torch
+from scipy import special, stats
+
+import ancestral_draft_sampling_gb300 as pkg
+import oracle
+from ancestral_draft_sampling_gb300 import workloads as wl
+from tests.parity import (check_block_against_oracle, default_rows, run_draft,
+                          to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def _np(out):
+    return tuple(t.cpu().numpy() for t in out)
+
+
+# ------------------------------------------------------------------ noise
+@pytest.mark.parametrize("seed,offset,k,stream", [
+    (0, 0, 0, 0), (1234, 0, 3, 0), (2**64 - 1, 2**40 + 7, 6, 0),
+    (99, 5, 2, 1), (99, 5, 7, 2)])
+def test_noise_words_bit_exact(seed, offset, k, stream):
+    n = 4099
+    words, g = pkg.noise_words(seed, offset, k, stream, n)
+    words = words.cpu().numpy().view(np.uint32)
+    ref = np.array([oracle.noise_word(seed, offset, k, stream, v)
+                    for v in range(n)], dtype=np.uint32)
+    np.testing.assert_array_equal(words, ref)
+    g = g.cpu().numpy()
+    gref = np.array([oracle.gumbel(int(x)) for x in ref])
+    # float32 log1pf/logf: a few ulp of |g| (|g| < 23)
+    np.testing.assert_allclose(g, gref, rtol=0, atol=4 * 2.0**-19)
+
+
+def test_gumbel_tails_bit_for_word():
+    """The words at both ends of the range give the extreme Gumbel values."""
+    # find words near 0 and near 2^32 among a long stream
+    n = 1 << 20
+    words, g = pkg.noise_words(77, 0, 0, 0, n)
+    words = words.cpu().numpy().view(np.uint32)
+    g = g.cpu().numpy()
+    for i in [int(np.argmin(words)), int(np.argmax(words))]:
+        assert abs(g[i] - oracle.gumbel(int(words[i]))) <= 4 * 2.0**-19
+
+
+# ------------------------------------------------------- small-shape parity
+SMALL_CASES = [
+    # B, K, V, r, base dtype, w dtype, T, extra
+    (1, 3, 4096, 64, wl.F32, wl.F32, 1.0, {}),
+    (3, 4, 4100, 32, wl.BF16, wl.BF16, 0.7, {}),          # ragged V (not /8)
+    (2, 2, 4099, 16, wl.F32, wl.BF16, 1.3, {}),           # odd V: scalar path
+    (5, 3, 1000, 48, wl.BF16, wl.F32, 1.0, {"greedy_rows": [1, 3]}),
+    (4, 3, 3000, 64, wl.F32, wl.BF16, 1.0, {"pad_rows": [0, 3]}),
+    (70, 2, 2048, 32, wl.BF16, wl.BF16, 1.0, {"n_spikes": 4}),  # two groups
+    (2, 3, 1536, 64, wl.F32, wl.F32, 0.05, {}),           # extreme T
+    (2, 3, 1536, 64, wl.F32, wl.F32, 20.0, {}),
+    (1, 1, 1, 16, wl.F32, wl.F32, 1.0, {}),               # V = 1
+    (3, 2, 130, 256, wl.BF16, wl.BF16, 1.0, {}),          # r = 256, V < 2 tiles
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")
+def test_small_parity(case):
+    B, K, V, r, bdt, wdt, T, extra = case
+    w = wl.make_custom(B, K, V, r, seed=100 + V + B, base_dtype=bdt,
+                       w_dtype=wdt, T=T, w_std=0.2, **extra)
+    base_before = w.base.copy()
+    dev = to_device(w)
+    tokens, logits, probs = _np(run_draft(w, dev))
+    stats_ = check_block_against_oracle(w, tokens, logits, probs)
+    assert stats_["near_tie_token_diffs"] <= 1
+    # the drafter's logits are left as they are
+    after = dev["base"].cpu()
+    if w.base.dtype == np.uint16:
+        after = after.view(torch.int16).numpy().view(np.uint16)
+    else:
+        after = after.numpy()
+    np.testing.assert_array_equal(after, base_before)
+
+
+def test_config_small_parity():
+    w = wl.make_config(1)
+    tokens, logits, probs = _np(run_draft(w))
+    st = check_block_against_oracle(w, tokens, logits, probs)
+    assert st["near_tie_token_diffs"] == 0
+    ref = oracle.draft_block(w.base, w.U, w.Wb, w.d0, w.seed, w.offset, w.T)
+    np.testing.assert_array_equal(tokens, ref.tokens)
+
+
+def test_greedy_ties_lowest_index():
+    B, K, V, r = 2, 2, 640, 16
+    w = wl.make_custom(B, K, V, r, seed=3, w_std=0.0, greedy_rows=[0, 1])
+    w.base[:] = 0.0
+    w.base[0, 0, [300, 17, 600]] = 5.0
+    w.base[1, :, :] = 1.0  # all equal -> index 0
+    tokens, logits, probs = _np(run_draft(w))
+    assert tokens[0, 0] == 17
+    assert (tokens[1] == 0).all()
+    assert probs[0, 0, 17] == 1.0 and probs[0, 0].sum() == 1.0
+
+
+def test_nan_valid_row_gives_legal_token():
+    w = wl.make_custom(2, 2, 900, 16, seed=4)
+    w.base[0, 0, ::3] = np.nan
+    w.base[1, :, :] = np.nan  # a valid (non-padding) row of NaN
+    tokens, logits, probs = _np(run_draft(w))
+    assert ((tokens >= 0) & (tokens < w.V)).all()
+    assert (tokens[1] == 0).all()
+    ref = oracle.draft_block(w.base, w.U, w.Wb, w.d0, w.seed, w.offset, w.T)
+    assert tokens[0, 0] == ref.tokens[0, 0]
+
+
+# --------------------------------------------------------- determinism
+def test_repeat_and_graph_replay_bitwise_and_new_offset():
+    w = wl.make_custom(6, 4, 5000, 64, seed=9, base_dtype=wl.BF16,
+                       w_dtype=wl.BF16, w_std=0.2, greedy_rows=[2])
+    dev = to_device(w)
+    ws = pkg.DraftWorkspace(w.B, w.K, w.V, w.r)
+    eager1 = _np(run_draft(w, dev, workspace=ws))
+    eager2 = _np(run_draft(w, dev, workspace=ws))
+    for a, b in zip(eager1, eager2):
+        np.testing.assert_array_equal(a, b)
+    # CUDA-graph capture of the whole C-ABI call, then replay
+    s = torch.cuda.Stream()
+    outs = [torch.empty_like(t) for t in (torch.empty((w.B, w.K), dtype=torch.int32, device="cuda"),
+                                          torch.empty((w.B, w.K, w.V), device="cuda"),
+                                          torch.empty((w.B, w.K, w.V), device="cuda"))]
+    call = lambda: pkg.draft_block(dev["base"], dev["U"], dev["Wb"], dev["d0"],
+                                   dev["seed"], dev["offset"], w.T,
+                                   greedy=dev["greedy"], tokens=outs[0],
+                                   logits=outs[1], draft_probs=outs[2],
+                                   workspace=ws, stream=s)
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()  # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for t in outs:
+        t.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager1, outs):
+        np.testing.assert_array_equal(a, b.cpu().numpy())
+    # a new offset draws anew (sampled rows), greedy row unchanged
+    dev["offset"].add_(1)
+    g.replay()
+    torch.cuda.synchronize()
+    t_new = outs[0].cpu().numpy()
+    sampled = [b for b in range(w.B) if b != 2]
+    assert (t_new[sampled] != eager1[0][sampled]).any()
+    np.testing.assert_array_equal(t_new[2], eager1[0][2])
+
+
+# ---------------------------------------------------------- distribution
+def _chi2(tokens, probs):
+    counts = np.bincount(tokens, minlength=len(probs)).astype(np.float64)
+    exp = probs * counts.sum()
+    keep = exp > 5
+    c = np.append(counts[keep], counts[~keep].sum())
+    e = np.append(exp[keep], exp[~keep].sum())
+    if e[-1] == 0:
+        c, e = c[:-1], e[:-1]
+    return stats.chisquare(c, e).pvalue
+
+
+@pytest.mark.parametrize("bdt", [wl.F32, wl.BF16])
+def test_draws_follow_softmax_and_condition_on_previous(bdt):
+    """Position 0 frequencies match softmax(l0 / T) and the joint (d0, d1)
+    matches softmax(l0)[a] softmax(l1 | a)[b] (chi-square p = 1e-4), over
+    many requests with distinct seeds, with the vocabulary split in several
+    chunks."""
+    V, r, K, T = 384, 16, 2, 0.9
+    B, calls = 1024, 120
+    rng = np.random.Generator(np.random.PCG64(int(bdt) + 5))
+    base_rows = (rng.standard_normal((K, V)) * 0.6).astype(np.float32)
+    base_rows[:, :6] += 3.0  # a few heavy tokens
+    U = (rng.standard_normal((V, r)) * 0.6).astype(np.float32)
+    Wb = (rng.standard_normal((r, V)) * 0.6).astype(np.float32)
+    if bdt == wl.BF16:
+        base_np = wl.to_bf16_bits(np.broadcast_to(base_rows, (B, K, V)).copy())
+        base_f = wl.bf16_bits_to_f32(base_np[0])
+    else:
+        base_np = np.broadcast_to(base_rows, (B, K, V)).copy()
+        base_f = base_rows
+    w = wl.Workload("chi2", B, K, V, r, T, base_np, U, Wb,
+                    np.full(B, 5, np.int32), np.zeros(B, np.uint64),
+                    np.zeros(B, np.uint64))
+    dev = to_device(w)
+    toks = []
+    for c in range(calls):
+        dev["seed"].copy_(torch.arange(B, dtype=torch.int64) + c * B + 17)
+        toks.append(run_draft(w, dev)[0].cpu().numpy())
+    toks = np.concatenate(toks)
+    U64, W64 = U.astype(np.float64), Wb.astype(np.float64)
+    l0 = (base_f[0].astype(np.float64) + U64[5] @ W64).astype(np.float32)
+    p0 = special.softmax((l0 / np.float32(T)).astype(np.float64))
+    assert _chi2(toks[:, 0], p0) > 1e-4
+    heavy = np.argsort(-p0)[:3]
+    for a in heavy:  # position 1 given the drawn position 0
+        l1 = (base_f[1].astype(np.float64) + U64[a] @ W64).astype(np.float32)
+        p1 = special.softmax((l1 / np.float32(T)).astype(np.float64))
+        m = toks[:, 0] == a
+        assert _chi2(toks[m, 1], p1) > 1e-4
+
+
+# ------------------------------------------------------- full-size configs
+@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
+def test_full_config_sampled_parity(cfg):
+    w = wl.make_config(cfg)
+    tokens, logits, probs = _np(run_draft(w))
+    rows = default_rows(w.B, w.K, max_rows=max(w.B, 96), seed=cfg)
+    st = check_block_against_oracle(w, tokens, logits, probs, rows=rows)
+    assert st["near_tie_token_diffs"] <= 1
+    # properties that hold at any size, on every row
+    assert ((tokens >= 0) & (tokens < w.V)).all()
+    sums = probs.astype(np.float64).sum(-1)
+    np.testing.assert_allclose(sums, 1.0, rtol=0, atol=1e-4)
+    assert np.isfinite(probs).all()
+    if w.greedy is not None:
+        g = np.flatnonzero(w.greedy)
+        s = logits[g] / np.float32(w.T)
+        np.testing.assert_array_equal(tokens[g], s.argmax(-1))
