@@ -9,6 +9,7 @@
 // so the whole call can be captured in a CUDA graph.
 #include <atomic>
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "dspark_common.cuh"
@@ -134,14 +135,30 @@ cudaError_t proposals_adapter(const DraftArgs& a, int, int, cudaStream_t s) {
   return launch_proposals(a, s);
 }
 
+// Which position kernel runs: the tensor-core kernel when the shape allows
+// it, else the FFMA kernel.  DSPARK_POSITION_KERNEL=generic forces the FFMA
+// kernel (for comparisons); =tc fails with UNSUPPORTED where it cannot run.
+int position_kernel_choice(const DraftArgs& a) {
+  const char* env = std::getenv("DSPARK_POSITION_KERNEL");
+  const bool tc_ok = position_tc_supported(a);
+  if (env && std::strcmp(env, "generic") == 0) return 0;
+  if (env && std::strcmp(env, "tc") == 0) return tc_ok ? 1 : -1;
+  return tc_ok ? 1 : 0;
+}
+
 // The launch sequence of one draft block.
 dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
                         StageTimer* t) {
-  const int want = sm_count() < kMaxChunks ? sm_count() : kMaxChunks;
-  const int n_chunks = generic_chunks_used(a.V, want);
+  const int sms = sm_count() < kMaxChunks ? sm_count() : kMaxChunks;
+  const int choice = position_kernel_choice(a);
+  if (choice < 0) return DSPARK_ERR_UNSUPPORTED;
+  const bool tc = choice == 1;
+  const int want = tc ? position_tc_chunks(a.V, sms) : sms;
+  const int n_chunks = tc ? want : generic_chunks_used(a.V, want);
   for (int k = 0; k < a.K; ++k) {
-    dspark_status st =
-        timed_launch(t, 0, stream, launch_position_generic, a, k, want);
+    dspark_status st = timed_launch(
+        t, 0, stream, tc ? launch_position_tc : launch_position_generic, a, k,
+        want);
     if (st != DSPARK_OK) return st;
     st = timed_launch(t, 1, stream, launch_pick, a, k, n_chunks);
     if (st != DSPARK_OK) return st;

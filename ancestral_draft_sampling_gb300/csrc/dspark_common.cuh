@@ -194,6 +194,7 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int B, int K) {
 enum DeviceError : int {
   kDevErrNone = 0,
   kDevErrBadToken = 1,  // a d0 entry outside [0, V) (token 0 used instead)
+  kDevErrTimeout = 2,   // a bounded wait inside a kernel ran out
 };
 
 // ------------------------------------------------------- kernel launchers
@@ -221,6 +222,10 @@ struct DraftArgs {
 // Launch helpers (each returns the cudaGetLastError of its launch).
 cudaError_t launch_position_generic(const DraftArgs& a, int k, int n_chunks,
                                     cudaStream_t stream);
+bool position_tc_supported(const DraftArgs& a);
+int position_tc_chunks(int V, int sm_count);
+cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
+                               cudaStream_t stream);
 cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
                         cudaStream_t stream);
 cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream);

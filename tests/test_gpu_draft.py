@@ -69,7 +69,19 @@ SMALL_CASES = [
     (2, 3, 1536, 64, wl.F32, wl.F32, 20.0, {}),
     (1, 1, 1, 16, wl.F32, wl.F32, 1.0, {}),               # V = 1
     (3, 2, 130, 256, wl.BF16, wl.BF16, 1.0, {}),          # r = 256, V < 2 tiles
+    # shapes the tensor-core kernel takes (bf16 head, r % 64 == 0, V % 8 == 0)
+    (16, 3, 4096, 64, wl.F32, wl.BF16, 1.0, {}),
+    (5, 2, 1000, 128, wl.BF16, wl.BF16, 0.7, {"greedy_rows": [1]}),  # ragged tile
+    (33, 2, 2056, 256, wl.F32, wl.BF16, 1.0, {"pad_rows": [0, 32]}),
+    (128, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),        # largest batch
+    (97, 1, 8192, 192, wl.F32, wl.BF16, 1.3, {}),
+    (1, 3, 200064, 256, wl.BF16, wl.BF16, 1.0, {"n_spikes": 32}),
 ]
+
+
+def tc_eligible(case):
+    B, K, V, r, bdt, wdt = case[:6]
+    return wdt == wl.BF16 and r % 64 == 0 and V % 8 == 0 and B <= 128
 
 
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")
@@ -89,6 +101,28 @@ def test_small_parity(case):
     else:
         after = after.numpy()
     np.testing.assert_array_equal(after, base_before)
+
+
+@pytest.mark.parametrize("case", [c for c in SMALL_CASES if tc_eligible(c)],
+                         ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")
+def test_ffma_kernel_parity_on_tensor_core_shapes(case, monkeypatch):
+    """The FFMA position kernel, forced on shapes the tensor-core kernel
+    normally takes, meets the same bar."""
+    monkeypatch.setenv("DSPARK_POSITION_KERNEL", "generic")
+    B, K, V, r, bdt, wdt, T, extra = case
+    w = wl.make_custom(B, K, V, r, seed=200 + V + B, base_dtype=bdt,
+                       w_dtype=wdt, T=T, w_std=0.2, **extra)
+    tokens, logits, probs = _np(run_draft(w))
+    st = check_block_against_oracle(w, tokens, logits, probs,
+                                    rows=default_rows(B, K, max_rows=64))
+    assert st["near_tie_token_diffs"] <= 1
+
+
+def test_forcing_tensor_core_kernel_on_unsupported_shape_fails(monkeypatch):
+    monkeypatch.setenv("DSPARK_POSITION_KERNEL", "tc")
+    w = wl.make_custom(2, 2, 1001, 64, seed=5, w_dtype=wl.BF16)
+    with pytest.raises(pkg.DsparkError):
+        run_draft(w)
 
 
 def test_config_small_parity():
