@@ -59,22 +59,24 @@ __device__ __forceinline__ uint32_t word_of(uint4 w, int i) {
   return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
 }
 
-// Standard Gumbel variate g = -log(-log(1 - w)), w = (x + 0.5) * 2^-32, in
-// float32.  The exponential variate E = -log(1 - w) is formed from whichever
-// of w and 1 - w is at most one half, so that both tails keep full relative
-// precision: E = -log1p(-w) when w <= 1/2, and E = -log(1 - w) with
-// 1 - w = (~x + 0.5) * 2^-32 otherwise.  Both forms are exact rewrites of
-// the same quantity; only their rounding differs.
+// Standard exponential variate E = -log(1 - w), w = (x + 0.5) * 2^-32, in
+// float32 without branches.  1 - w = y * 2^-32 with y = ~x + 0.5; 2y is an
+// odd integer below 2^33, split exactly as hi + lo with hi = 2y rounded to
+// the nearest float32 and lo the integer remainder (|lo| <= 2^8), so that
+// log(2y) = log(hi) + log1p(lo / hi) and log1p(lo / hi) = lo / hi up to
+// (lo / hi)^2 / 2 <= 2^-51 (Dekker-style splitting of the argument).  Both
+// tails keep full relative precision: for w near 0, hi * 2^-33 is 1 or the
+// float just below it and the small lo / hi carries E; for w near 1, lo = 0.
+__device__ __forceinline__ float exponential_from_word(uint32_t x) {
+  const unsigned long long y2 = 2ull * (unsigned long long)(~x) + 1ull;
+  const float hi = __ull2float_rn(y2);
+  const int lo = (int)((long long)y2 - (long long)__float2ull_rn(hi));
+  return -(logf(hi * 0x1p-33f) + __fdividef((float)lo, hi));
+}
+
+// Standard Gumbel variate g = -log(E) = -log(-log(1 - w)).
 __device__ __forceinline__ float gumbel_from_word(uint32_t x) {
-  float e;
-  if (x < 0x80000000u) {
-    const float w = fmaf((float)x, 0x1p-32f, 0x1p-33f);
-    e = -log1pf(-w);
-  } else {
-    const float one_minus_w = fmaf((float)(~x), 0x1p-32f, 0x1p-33f);
-    e = -logf(one_minus_w);
-  }
-  return -logf(e);
+  return -logf(exponential_from_word(x));
 }
 
 // Uniform in (0, 1) for the acceptance test, exact in float32:
@@ -87,8 +89,8 @@ __device__ __forceinline__ float accept_uniform(uint32_t x) {
 // Per (request, vocab chunk): the best decision score and its index, and the
 // running (max m, sum exp(s - m)) of the scaled logits.
 struct alignas(16) ChunkStat {
-  float best;  // largest non-NaN decision score (s + g, or s for greedy)
-  int idx;     // its lowest index; kNoIndex if every score was NaN
+  float best;  // largest decision score (s + g, or s for greedy rows)
+  int idx;     // its lowest index; kNoIndex if no score beat -inf
   float m;     // max of the non-NaN scaled logits (-inf if none)
   float s;     // sum of exp(s_v - m) (NaN if any s_v was NaN)
 };

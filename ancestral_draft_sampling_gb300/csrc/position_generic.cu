@@ -96,7 +96,7 @@ __device__ __forceinline__ void fold4(ChunkStat& st, const float s[4],
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     if (v + e >= V) continue;
-    if (!isnan(score[e]) && (st.idx == kNoIndex || score[e] > st.best)) {
+    if (score[e] > st.best) {  // NaN and -inf never win
       st.best = score[e];
       st.idx = v + e;
     }

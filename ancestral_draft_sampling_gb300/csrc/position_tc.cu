@@ -40,7 +40,7 @@ constexpr int kTileV = 128;                        // vocab rows per tile (M)
 constexpr int kKChunk = 64;                        // r per pipeline stage
 constexpr int kBoxBytes = 64 * kKChunk * 2;        // one 64x64 bf16 box
 constexpr int kStageBytes = 2 * kBoxBytes;         // 128 vocab x 64 r
-constexpr int kComputeWarps = 8;
+constexpr int kComputeWarps = 16;
 constexpr int kThreads = 32 * (2 + kComputeWarps);
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kMaxBpad = 128;
@@ -50,6 +50,7 @@ constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSpin = 1u << 22;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;              // 227 KB per CTA
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct RowInfo {
   uint64_t seed;
@@ -68,38 +69,59 @@ struct TcParams {
   uint32_t u_off, bias_off, rows_off, bar_off;
 };
 
+// Running state of one (lane, request) over the lane's vocab entries:
+//   m    max of the scaled logits s seen (-inf if none);
+//   sum  sum of exp(s - m);
+//   key  the best candidate so far, relative to m: exp(s - m) / E for a
+//        sampled request (exponential race: the largest exp(s) / E is the
+//        largest s - log E = s + g), s itself for a greedy request;
+//   idx  its vocab index (kNoIndex while nothing has won).
+struct LaneStat {
+  float m, sum, key;
+  int idx;
+};
+
 __device__ __forceinline__ void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ float scale(float l, float T) {
   return T == 1.0f ? l : __fdiv_rn(l, T);
 }
 
-__device__ __forceinline__ void fold4(ChunkStat& st, const float s[4],
-                                      const float score[4], int v, int V) {
-  float m4 = -INFINITY;
-  bool any_nan = false;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (v + e >= V) continue;
-    if (!isnan(score[e]) && (st.idx == kNoIndex || score[e] > st.best)) {
-      st.best = score[e];
-      st.idx = v + e;
-    }
-    m4 = fmaxf(m4, s[e]);
-    any_nan |= isnan(s[e]);
-  }
+// Folds the four candidates v..v+3 (s[e] = -inf past V) into st.  E is the
+// exponential variate of each candidate (unused for greedy requests).
+template <bool kGreedy>
+__device__ __forceinline__ void fold4(LaneStat& st, const float s[4],
+                                      const float E[4], int v) {
+  const float m4 = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
   const float mn = fmaxf(st.m, m4);
-  if (mn == -INFINITY) {
-    if (any_nan) st.s = __int_as_float(0x7fc00000);
-  } else {
-    float acc = (st.m == mn) ? st.s : __fmul_rn(st.s, expf(st.m - mn));
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (v + e < V) acc = __fadd_rn(acc, expf(s[e] - mn));
-    st.s = acc;
+  if (mn > st.m) {  // a new running max: rescale what is kept relative to m
+    const float f = ex2_approx((st.m - mn) * kLog2e);
+    st.sum *= f;
+    if (!kGreedy) st.key *= f;
     st.m = mn;
+  }
+  if (mn != -INFINITY) {
+    const float nml = -mn * kLog2e;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float ee = ex2_approx(fmaf(s[e], kLog2e, nml));
+      st.sum += ee;
+      const float key = kGreedy ? s[e] : __fdividef(ee, E[e]);
+      if (key > st.key) {  // strict: the lower index keeps a tie
+        st.key = key;
+        st.idx = v + e;
+      }
+    }
+  } else if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3])) {
+    st.sum = __int_as_float(0x7fc00000);
   }
 }
 
@@ -114,6 +136,26 @@ __device__ __forceinline__ void load_base4(const BT* p, float out[4]) {
     out[1] = __uint_as_float(x.x & 0xffff0000u);
     out[2] = __uint_as_float(x.y << 16);
     out[3] = __uint_as_float(x.y & 0xffff0000u);
+  }
+}
+
+template <int kN>
+__device__ __forceinline__ void tmem_ld4x(uint32_t taddr, float (&v)[4 * kN],
+                                          int n_valid) {
+#pragma unroll
+  for (int i = 0; i < kN; ++i) {
+    if (i < n_valid) {
+      uint32_t r0, r1, r2, r3;
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+          : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+          : "r"(taddr + 4u * i)
+          : "memory");
+      v[4 * i] = __uint_as_float(r0);
+      v[4 * i + 1] = __uint_as_float(r1);
+      v[4 * i + 2] = __uint_as_float(r2);
+      v[4 * i + 3] = __uint_as_float(r3);
+    }
   }
 }
 
@@ -158,7 +200,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4 * 32);
+      mbar_init(&acc_empty[i], kComputeThreads);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
@@ -290,47 +332,55 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   } else {
     // ----------------------------------------------------------- compute
     const int cw = warp - 2;
-    const bool drainer = cw < 4;
-    const int quarter = warp & 3;  // TMEM lanes this warp may access
-    const int rpw = P.bpad / kComputeWarps;
+    const int quarter = warp & 3;        // TMEM lanes this warp may access
+    const int col_group = cw >> 2;       // which quarter of the columns
+    const int cols = P.bpad / 4;         // columns drained by this warp
+    const int col0 = col_group * cols;
     const BT* base = static_cast<const BT*>(a.base);
     const float T = a.T;
     const int V = a.V;
-    ChunkStat st[kMaxRowsPerWarp];
+    LaneStat st[kMaxRowsPerWarp];
 #pragma unroll
-    for (int i = 0; i < kMaxRowsPerWarp; ++i) st[i] = empty_stat();
+    for (int i = 0; i < kMaxRowsPerWarp; ++i) {
+      st[i].m = -INFINITY;
+      st[i].sum = 0.0f;
+      st[i].key = 0.0f;
+      st[i].idx = kNoIndex;
+    }
+#pragma unroll
+    for (int i = 0; i < kMaxRowsPerWarp; ++i) {
+      const int b = cw + kComputeWarps * i;
+      if (b < a.B && rows[b].greedy) st[i].key = -INFINITY;
+    }
 
     for (int t = 0; t < n_tiles; ++t) {
       const int acc = t & 1;
       const uint32_t aph = (uint32_t)(t >> 1) & 1u;
-      if (drainer) {
-        bool ok = !*abort_flag && mbar_wait(&acc_full[acc], aph, kSpin);
-        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
-        if (!ok) {
-          if (!*abort_flag) fail(kDevErrTimeout);
-        } else {
-          tc_fence_after();
-          const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                                 (uint32_t)acc * kAccCols;
-          const int m = quarter * 32 + lane;
-          for (int c0 = 0; c0 < P.bpad; c0 += 16) {
-            float vals[16];
-            tmem_ld16(taddr + (uint32_t)c0, vals);
-            tmem_ld_wait();
+      // drain: lanes quarter*32.., columns col0..col0+cols of the accumulator
+      bool ok = !*abort_flag && mbar_wait(&acc_full[acc], aph, kSpin);
+      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
+      if (ok) {
+        tc_fence_after();
+        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
+                               (uint32_t)acc * kAccCols + (uint32_t)col0;
+        float vals[kMaxBpad / 4];
+        tmem_ld4x<kMaxBpad / 16>(taddr, vals, cols / 4);
+        tmem_ld_wait();
+        const int m = quarter * 32 + lane;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) bias_s[(c0 + i) * kTileV + m] = vals[i];
-          }
-          tc_fence_before();
-        }
-        mbar_arrive(&acc_empty[acc]);
+        for (int i = 0; i < kMaxBpad / 4; ++i)
+          if (i < cols) bias_s[(col0 + i) * kTileV + m] = vals[i];
+        tc_fence_before();
+      } else if (!*abort_flag) {
+        fail(kDevErrTimeout);
       }
+      mbar_arrive(&acc_empty[acc]);
       named_sync(1, kComputeThreads);  // bias tile complete
       if (!*abort_flag) {
         const int v = (t_begin + t) * kTileV + 4 * lane;
         const bool valid = v < V;  // V % 8 == 0: v..v+3 all in range
 #pragma unroll
         for (int i = 0; i < kMaxRowsPerWarp; ++i) {
-          if (i >= rpw) break;
           const int b = cw + kComputeWarps * i;
           if (b >= a.B) break;
           const RowInfo ri = rows[b];
@@ -339,38 +389,62 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
               *reinterpret_cast<const float4*>(bias_s + b * kTileV + 4 * lane);
           float b4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
           if (!ri.pad && valid) load_base4<BT>(base + row * V + v, b4);
-          float l[4], s[4], score[4];
+          float l[4], s[4];
           l[0] = ri.pad ? bias.x : __fadd_rn(b4[0], bias.x);
           l[1] = ri.pad ? bias.y : __fadd_rn(b4[1], bias.y);
           l[2] = ri.pad ? bias.z : __fadd_rn(b4[2], bias.z);
           l[3] = ri.pad ? bias.w : __fadd_rn(b4[3], bias.w);
-          if (valid)
+          if (valid) {
             __stcs(reinterpret_cast<float4*>(a.logits + row * V + v),
                    make_float4(l[0], l[1], l[2], l[3]));
 #pragma unroll
-          for (int e = 0; e < 4; ++e) s[e] = scale(l[e], T);
-          if (ri.greedy) {
+            for (int e = 0; e < 4; ++e) s[e] = scale(l[e], T);
+          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) score[e] = s[e];
+            for (int e = 0; e < 4; ++e) s[e] = -INFINITY;
+          }
+          if (ri.greedy) {
+            float E[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+            fold4<true>(st[i], s, E, v);
           } else {
             const uint4 w = noise_block(ri.seed, ri.offset, P.k, kNoiseDraft,
                                         (uint32_t)v >> 2);
-            score[0] = __fadd_rn(s[0], gumbel_from_word(w.x));
-            score[1] = __fadd_rn(s[1], gumbel_from_word(w.y));
-            score[2] = __fadd_rn(s[2], gumbel_from_word(w.z));
-            score[3] = __fadd_rn(s[3], gumbel_from_word(w.w));
+            float E[4];
+            E[0] = exponential_from_word(w.x);
+            E[1] = exponential_from_word(w.y);
+            E[2] = exponential_from_word(w.z);
+            E[3] = exponential_from_word(w.w);
+            fold4<false>(st[i], s, E, v);
           }
-          fold4(st[i], s, score, v, V);
         }
       }
       named_sync(2, kComputeThreads);  // bias tile consumed
     }
+    // chunk statistics: the lane winner's log-domain score s + g, then a
+    // butterfly over the warp
 #pragma unroll
     for (int i = 0; i < kMaxRowsPerWarp; ++i) {
-      if (i >= rpw) break;
       const int b = cw + kComputeWarps * i;
       if (b >= a.B) break;
-      const ChunkStat red = warp_reduce_stat(st[i]);
+      const RowInfo ri = rows[b];
+      ChunkStat cs;
+      cs.idx = st[i].idx;
+      cs.m = st[i].m;
+      cs.s = st[i].sum;
+      cs.best = -INFINITY;
+      if (cs.idx != kNoIndex) {
+        if (ri.greedy) {
+          cs.best = st[i].key;
+        } else {
+          const size_t row = (size_t)b * a.K + P.k;
+          const float s_best = scale(a.logits[row * V + cs.idx], T);
+          const uint4 w = noise_block(ri.seed, ri.offset, P.k, kNoiseDraft,
+                                      (uint32_t)cs.idx >> 2);
+          cs.best = __fadd_rn(
+              s_best, -logf(exponential_from_word(word_of(w, cs.idx & 3))));
+        }
+      }
+      const ChunkStat red = warp_reduce_stat(cs);
       if (lane == 0) a.stats[(size_t)b * kMaxChunks + chunk] = red;
     }
   }

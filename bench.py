@@ -94,7 +94,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
@@ -261,6 +261,9 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl")
 
     w = wl.make_config(CONFIG_ID)
+    if args.positions != w.K:
+        w.K = args.positions
+        w.base = np.ascontiguousarray(w.base[:, :w.K])
     dev = to_device(w, f"cuda:{local}")
     B, K, V, r = w.B, w.K, w.V, w.r
     tokens = torch.empty((B, K), dtype=torch.int32, device="cuda")
@@ -273,6 +276,12 @@ def run_ours(args, rank, world):
                         dev["offset"], w.T, greedy=dev["greedy"],
                         pad_row=dev["pad_row"], tokens=tokens, logits=logits,
                         draft_probs=probs, workspace=ws, stream=stream)
+
+    if args.mode == "ncu":
+        for _ in range(args.blocks):
+            call()
+        torch.cuda.synchronize()
+        return 0
 
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -400,10 +409,18 @@ def run_ours(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", choices=["bench", "ncu"], default="bench",
+                    help="ncu: run a few eager blocks and exit (a small, "
+                         "self-ending workload for profiler captures)")
+    ap.add_argument("--positions", type=int, default=7,
+                    help="draft positions K (7 = the benchmark workload; "
+                         "fewer shrink the device footprint for captures)")
+    ap.add_argument("--blocks", type=int, default=2,
+                    help="eager blocks run by --mode ncu")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -21,7 +21,8 @@
  * (v >> 2, k | stream << 16, offset lo, offset hi), word v & 3; stream 0
  * feeds the draft, 1 the acceptance uniforms, 2 the residual / bonus draws.
  * g = -log(-log1p(-w)), w = (x + 0.5) * 2^-32.  Ties go to the lowest index;
- * a NaN score never wins (a row whose scores are all NaN yields token 0).
+ * a NaN or -inf score never wins, and a row where nothing wins (every score
+ * NaN or -inf) yields token 0.
  *
  * Conventions for every entry point:
  *   - All tensors are dense, row-major, and live in device memory unless

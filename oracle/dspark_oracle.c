@@ -37,7 +37,8 @@
  *     bit").  The perturbed score that decides the token is taken in the
  *     kernel's precision: g is computed in double and rounded once to float,
  *     and score = s + g is a float32 addition.  Ties go to the lowest index;
- *     a NaN score never wins.
+ *     a NaN or -inf score never wins, and a row where nothing wins draws
+ *     token 0.
  *   - Greedy rows consume no noise and store a one-hot proposal (PR #27,
  *     "Also checked": a greedy-sentinel row draws the argmax with a one-hot
  *     proposal).
@@ -183,8 +184,7 @@ int oracle_draft_position(const void* base_row, int base_dtype, int is_pad,
                                                        (uint32_t)v));
       score = s + g;
     }
-    if (isnan(score)) continue;
-    if (!found || score > best) {
+    if (score > best) { /* NaN and -inf never win; ties keep the lower v */
       best = score;
       token = v;
       found = 1;

@@ -356,3 +356,26 @@ def test_verification_zero_target_rejects():
                                  np.zeros(N, np.uint64))
     assert (res.accepted_len == 0).all()
     assert (res.emitted != 0).all()
+
+
+def test_nan_and_minus_inf_never_win():
+    """Reading where the pages are silent: a NaN or -inf score never wins,
+    ties keep the lower index, and a row where nothing wins draws token 0."""
+    V, r = 6, 4
+    U = np.zeros((V, r), np.float32)
+    Wb = np.zeros((r, V), np.float32)
+    inf, nan = np.float32(np.inf), np.float32(np.nan)
+    rows = np.array([
+        [[-inf, nan, 2.0, 2.0, nan, -inf]],   # greedy: 2 (tie -> lower index)
+        [[-inf] * V],                          # nothing wins -> 0
+        [[nan] * V],                           # nothing wins -> 0
+        [[nan, -inf, nan, -inf, nan, -inf]],   # nothing wins -> 0
+    ], dtype=np.float32)
+    for row, want in zip(rows, [2, 0, 0, 0]):
+        out = oracle.draft_block(row[None], U, Wb, [1], [3], [0], 1.0, greedy=[1])
+        assert out.tokens[0, 0] == want
+        out = oracle.draft_block(row[None], U, Wb, [1], [3], [0], 1.0)
+        if want == 2:
+            assert out.tokens[0, 0] in (2, 3)  # sampled: one of the finite ones
+        else:
+            assert out.tokens[0, 0] == 0
