@@ -36,11 +36,11 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 ctr, uint2 key) {
       key.x += 0x9E3779B9u;
       key.y += 0xBB67AE85u;
     }
-    const uint32_t lo_a = 0xD2511F53u * ctr.x;
-    const uint32_t hi_a = __umulhi(0xD2511F53u, ctr.x);
-    const uint32_t lo_b = 0xCD9E8D57u * ctr.z;
-    const uint32_t hi_b = __umulhi(0xCD9E8D57u, ctr.z);
-    ctr = make_uint4(hi_b ^ ctr.y ^ key.x, lo_b, hi_a ^ ctr.w ^ key.y, lo_a);
+    // one widening multiply gives both halves of each 64-bit product
+    const unsigned long long pa = (unsigned long long)0xD2511F53u * ctr.x;
+    const unsigned long long pb = (unsigned long long)0xCD9E8D57u * ctr.z;
+    ctr = make_uint4((uint32_t)(pb >> 32) ^ ctr.y ^ key.x, (uint32_t)pb,
+                     (uint32_t)(pa >> 32) ^ ctr.w ^ key.y, (uint32_t)pa);
   }
   return ctr;
 }
@@ -60,18 +60,23 @@ __device__ __forceinline__ uint32_t word_of(uint4 w, int i) {
 }
 
 // Standard exponential variate E = -log(1 - w), w = (x + 0.5) * 2^-32, in
-// float32 without branches.  1 - w = y * 2^-32 with y = ~x + 0.5; 2y is an
-// odd integer below 2^33, split exactly as hi + lo with hi = 2y rounded to
-// the nearest float32 and lo the integer remainder (|lo| <= 2^8), so that
-// log(2y) = log(hi) + log1p(lo / hi) and log1p(lo / hi) = lo / hi up to
-// (lo / hi)^2 / 2 <= 2^-51 (Dekker-style splitting of the argument).  Both
-// tails keep full relative precision: for w near 0, hi * 2^-33 is 1 or the
-// float just below it and the small lo / hi carries E; for w near 1, lo = 0.
+// float32 with one logarithm and no divergent branch.  Both w and 1 - w are
+// formed from the word (exact up to one rounding), and the logarithm is
+// taken of whichever is the better argument:
+//   w >= 1/2: E = -log(1 - w), 1 - w = (~x + 0.5) * 2^-32 <= 1/2;
+//   w <  1/2: E = -log1p(-w) by Kahan's identity log1p(z) = z log(u)/(u - 1)
+//             with u = 1 + z rounded (u - 1 is exact for u in [1/2, 1]), and
+//             E = w when u rounds to 1.
+// Relative error a few ulp over the whole range, including both tails.
 __device__ __forceinline__ float exponential_from_word(uint32_t x) {
-  const unsigned long long y2 = 2ull * (unsigned long long)(~x) + 1ull;
-  const float hi = __ull2float_rn(y2);
-  const int lo = (int)((long long)y2 - (long long)__float2ull_rn(hi));
-  return -(logf(hi * 0x1p-33f) + __fdividef((float)lo, hi));
+  const bool lower = x < 0x80000000u;
+  const float w = fmaf(__uint2float_rn(x), 0x1p-32f, 0x1p-33f);
+  const float one_minus_w = fmaf(__uint2float_rn(~x), 0x1p-32f, 0x1p-33f);
+  const float u = lower ? __fsub_rn(1.0f, w) : one_minus_w;
+  const float L = logf(u);
+  const float d = __fsub_rn(u, 1.0f);
+  const float kahan = d == 0.0f ? w : __fmul_rn(L, __fdividef(w, d));
+  return lower ? kahan : -L;
 }
 
 // Standard Gumbel variate g = -log(E) = -log(-log(1 - w)).

@@ -64,6 +64,7 @@ struct TcParams {
   int k;
   int bpad;
   int stages;
+  int nbuf;  // bias tiles in shared memory (2: drain of t+1 overlaps t)
   int tiles_total;
   int n_chunks;
   uint32_t u_off, bias_off, rows_off, bar_off;
@@ -115,13 +116,44 @@ __device__ __forceinline__ void fold4(LaneStat& st, const float s[4],
       const float ee = ex2_approx(fmaf(s[e], kLog2e, nml));
       st.sum += ee;
       const float key = kGreedy ? s[e] : __fdividef(ee, E[e]);
-      if (key > st.key) {  // strict: the lower index keeps a tie
-        st.key = key;
-        st.idx = v + e;
-      }
+      const bool win = key > st.key;  // strict: the lower index keeps a tie
+      st.key = win ? key : st.key;
+      st.idx = win ? v + e : st.idx;
     }
   } else if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3])) {
     st.sum = __int_as_float(0x7fc00000);
+  }
+}
+
+// One request's four vocab entries v..v+3 of the tile: biased logits (written
+// when `store`), scaled logits, noise, and the fold into the lane state.
+__device__ __forceinline__ void process_row(const RowInfo& ri, size_t row,
+                                            const float4 bias, const float x[4],
+                                            bool valid, bool store, int v,
+                                            LaneStat& st, const DraftArgs& a,
+                                            int k, float T) {
+  float l[4], s[4];
+  l[0] = ri.pad ? bias.x : __fadd_rn(x[0], bias.x);
+  l[1] = ri.pad ? bias.y : __fadd_rn(x[1], bias.y);
+  l[2] = ri.pad ? bias.z : __fadd_rn(x[2], bias.z);
+  l[3] = ri.pad ? bias.w : __fadd_rn(x[3], bias.w);
+  if (valid && store)
+    __stcs(reinterpret_cast<float4*>(a.logits + row * a.V + v),
+           make_float4(l[0], l[1], l[2], l[3]));
+#pragma unroll
+  for (int e = 0; e < 4; ++e) s[e] = valid ? scale(l[e], T) : -INFINITY;
+  if (ri.greedy) {
+    const float E[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+    fold4<true>(st, s, E, v);
+  } else {
+    const uint4 w = noise_block(ri.seed, ri.offset, k, kNoiseDraft,
+                                (uint32_t)v >> 2);
+    float E[4];
+    E[0] = exponential_from_word(w.x);
+    E[1] = exponential_from_word(w.y);
+    E[2] = exponential_from_word(w.z);
+    E[3] = exponential_from_word(w.w);
+    fold4<false>(st, s, E, v);
   }
 }
 
@@ -356,6 +388,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int t = 0; t < n_tiles; ++t) {
       const int acc = t & 1;
       const uint32_t aph = (uint32_t)(t >> 1) & 1u;
+      float* bias_t = bias_s + (P.nbuf == 2 ? acc : 0) * (P.bpad * kTileV);
       // drain: lanes quarter*32.., columns col0..col0+cols of the accumulator
       bool ok = !*abort_flag && mbar_wait(&acc_full[acc], aph, kSpin);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
@@ -369,13 +402,15 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         const int m = quarter * 32 + lane;
 #pragma unroll
         for (int i = 0; i < kMaxBpad / 4; ++i)
-          if (i < cols) bias_s[(col0 + i) * kTileV + m] = vals[i];
+          if (i < cols) bias_t[(col0 + i) * kTileV + m] = vals[i];
         tc_fence_before();
       } else if (!*abort_flag) {
         fail(kDevErrTimeout);
       }
       mbar_arrive(&acc_empty[acc]);
-      named_sync(1, kComputeThreads);  // bias tile complete
+      // bias tile complete (and, with two tiles, the other one is free again:
+      // every warp finished computing on it before arriving here)
+      named_sync(1, kComputeThreads);
       if (!*abort_flag) {
         const int v = (t_begin + t) * kTileV + 4 * lane;
         const bool valid = v < V;  // V % 8 == 0: v..v+3 all in range
@@ -384,41 +419,15 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           const int b = cw + kComputeWarps * i;
           if (b >= a.B) break;
           const RowInfo ri = rows[b];
-          const size_t row = (size_t)b * a.K + P.k;
           const float4 bias =
-              *reinterpret_cast<const float4*>(bias_s + b * kTileV + 4 * lane);
-          float b4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (!ri.pad && valid) load_base4<BT>(base + row * V + v, b4);
-          float l[4], s[4];
-          l[0] = ri.pad ? bias.x : __fadd_rn(b4[0], bias.x);
-          l[1] = ri.pad ? bias.y : __fadd_rn(b4[1], bias.y);
-          l[2] = ri.pad ? bias.z : __fadd_rn(b4[2], bias.z);
-          l[3] = ri.pad ? bias.w : __fadd_rn(b4[3], bias.w);
-          if (valid) {
-            __stcs(reinterpret_cast<float4*>(a.logits + row * V + v),
-                   make_float4(l[0], l[1], l[2], l[3]));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[e] = scale(l[e], T);
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) s[e] = -INFINITY;
-          }
-          if (ri.greedy) {
-            float E[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-            fold4<true>(st[i], s, E, v);
-          } else {
-            const uint4 w = noise_block(ri.seed, ri.offset, P.k, kNoiseDraft,
-                                        (uint32_t)v >> 2);
-            float E[4];
-            E[0] = exponential_from_word(w.x);
-            E[1] = exponential_from_word(w.y);
-            E[2] = exponential_from_word(w.z);
-            E[3] = exponential_from_word(w.w);
-            fold4<false>(st[i], s, E, v);
-          }
+              *reinterpret_cast<const float4*>(bias_t + b * kTileV + 4 * lane);
+          const size_t row = (size_t)b * a.K + P.k;
+          float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+          if (!ri.pad && valid) load_base4<BT>(base + row * V + v, x);
+          process_row(ri, row, bias, x, valid, true, v, st[i], a, P.k, T);
         }
       }
-      named_sync(2, kComputeThreads);  // bias tile consumed
+      if (P.nbuf == 1) named_sync(2, kComputeThreads);  // bias tile consumed
     }
     // chunk statistics: the lane winner's log-domain score s + g, then a
     // butterfly over the warp
@@ -474,11 +483,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct Layout {
-  int bpad, stages;
+  int bpad, stages, nbuf;
   uint32_t u_off, bias_off, rows_off, bar_off;
   size_t smem;
 };
 
+// Shared memory: the Wb ring, u, one or two bias tiles, row info, barriers.
+// Two bias tiles are used when at least four ring stages still fit.
 Layout make_layout(int B, int r) {
   Layout L;
   L.bpad = (B + 15) / 16 * 16;
@@ -486,12 +497,15 @@ Layout make_layout(int B, int r) {
   const size_t bias = (size_t)L.bpad * kTileV * 4;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowInfo), 16);
   const size_t bars_max = (2 * kMaxStages + 5) * 8 + 16;
-  const size_t fixed = u + bias + rows + bars_max + 1024;
-  L.stages = (int)((kSmemLimit - fixed) / kStageBytes);
-  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  for (L.nbuf = 2; L.nbuf >= 1; --L.nbuf) {
+    const size_t fixed = u + L.nbuf * bias + rows + bars_max + 1024;
+    L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
+    if (L.stages > kMaxStages) L.stages = kMaxStages;
+    if (L.stages >= 4 || L.nbuf == 1) break;
+  }
   L.u_off = (uint32_t)((size_t)L.stages * kStageBytes);
   L.bias_off = (uint32_t)(L.u_off + u);
-  L.rows_off = (uint32_t)(L.bias_off + bias);
+  L.rows_off = (uint32_t)(L.bias_off + L.nbuf * bias);
   L.bar_off = (uint32_t)(L.rows_off + rows);
   L.smem = L.bar_off + (2 * L.stages + 5) * 8 + 16 + 1024;
   return L;
@@ -532,6 +546,7 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
   P.k = k;
   P.bpad = L.bpad;
   P.stages = L.stages;
+  P.nbuf = L.nbuf;
   P.tiles_total = (a.V + kTileV - 1) / kTileV;
   P.n_chunks = n_chunks;
   P.u_off = L.u_off;
