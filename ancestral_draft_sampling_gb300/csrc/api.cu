@@ -153,6 +153,8 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   const int choice = position_kernel_choice(a);
   if (choice < 0) return DSPARK_ERR_UNSUPPORTED;
   const bool tc = choice == 1;
+  // position kernels fill n_slots statistics slots per request; the pick
+  // merges them in slot order
   const int want = tc ? position_tc_chunks(a.V, sms) : sms;
   const int n_chunks = tc ? want : generic_chunks_used(a.V, want);
   for (int k = 0; k < a.K; ++k) {

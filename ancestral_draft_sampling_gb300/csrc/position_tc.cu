@@ -8,22 +8,34 @@
 // is fused into the position kernel.
 //
 // Per CTA (one per SM, a contiguous range of 128-wide vocab tiles):
-//   warp 0      TMA producer: Wb[r0:r0+64, v0:v0+128] stages (two 64x64
-//               boxes, 128-byte swizzle) into a ring of shared-memory stages.
-//   warp 1      MMA issuer: D[v, b] = sum_j Wb[j, v] * u[b, j] with
-//               tcgen05.mma kind::f16 (M = 128 vocab rows, N = B rounded up
-//               to 16, K = r), accumulating in one of two TMEM buffers.
-//               A (Wb tile) is vocab-major, B (u) is r-major.
-//   warps 2..9  compute.  Warps 2..5 (one per TMEM lane quarter) drain the
-//               finished accumulator into a [b][128] float32 shared tile;
-//               then all eight take requests b = w, w+8, ... with lane l on
-//               vocab entries 4l..4l+3 (one Philox block), add the drafter
-//               logits, write the float32 biased logits, scale, perturb and
-//               fold into per-lane running statistics, reduced per warp at
-//               the end of the chunk.
+//   warp 0, lane 0  TMA producer of Wb[r0:r0+64, v0:v0+128] stages (two
+//                   64x64 boxes, 128-byte swizzle) into a ring.
+//   warp 0, lane 1  TMA producer of the drafter-logit tile base[:, k,
+//                   v0:v0+128] ([Bpad x 128], rows past B read as zero),
+//                   straight into one of two float32 tile buffers (bf16
+//                   logits go to a staging tile instead).
+//   warp 1, lane 0  MMA issuer: D[v, b] = sum_j Wb[j, v] * u[b, j] with
+//                   tcgen05.mma kind::f16 (M = 128 vocab rows, N = B rounded
+//                   up to 16, K = r) into one of two TMEM accumulators.  A
+//                   (the Wb tile) is vocab-major, B (u) is r-major.
+//   warps 2..17     compute.  Warp (q, j), q = warp % 4, drains TMEM lanes
+//                   32q.. (vocab) of column group j (requests j*B/4 ..) and
+//                   writes l = base + bias (l = bias on padding rows) into
+//                   the tile buffer, in place.  After one barrier the tile
+//                   holds the float32 biased logits: one thread stores it to
+//                   global memory with a TMA tile store, and warp w takes
+//                   requests w, w+16, ... with lane L on vocab 4L .. 4L+3
+//                   (one Philox block): scaled logits, noise, the decision
+//                   and the sum-exp, all from shared memory.
+// Decision: a conservative test per entry (one exp2, no logarithm) admits
+// every entry that may beat the request's best score so far; only those get
+// the exact score s + g, merged over the warp by a butterfly.  The same
+// exp2 value, exp(s - best), feeds the sum-exp: the best score is the
+// reference of each request's running sum.
+//
 // Every mbarrier wait is bounded; on a timeout the kernel records an error
 // in the workspace control word, stops issuing work, waits (bounded) for
-// its in-flight MMAs, frees its TMEM and returns.
+// its in-flight copies and MMAs, frees its TMEM and returns.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -43,14 +55,22 @@ constexpr int kStageBytes = 2 * kBoxBytes;         // 128 vocab x 64 r
 constexpr int kComputeWarps = 16;
 constexpr int kThreads = 32 * (2 + kComputeWarps);
 constexpr int kComputeThreads = 32 * kComputeWarps;
-constexpr int kMaxBpad = 128;
-constexpr int kMaxRowsPerWarp = kMaxBpad / kComputeWarps;
+constexpr int kMaxBpad = 96;
+constexpr int kMaxRows = kMaxBpad / kComputeWarps; // requests per warp
 constexpr uint32_t kTmemCols = 256;                // two accumulators
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSpin = 1u << 22;
+constexpr int kMinStages = 3;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;              // 227 KB per CTA
 constexpr float kLog2e = 1.4426950408889634f;
+// Slack of the candidate test in log2 units: the test admits entries up to a
+// factor 2^(2^-11) = 1 + 3.4e-4 past the exact bound (32 + 2^-11 is exact in
+// float32).
+constexpr float kThrSlack = 0x1p-11f;
+// exp(s - best) from the test value 2^(32 + slack) exp(s - best): the scale
+// 2^-(32 + 2^-11), rounded to float32 (relative error < 2^-24)
+constexpr float kSumScale = 2.3275186e-10f;
 
 struct RowInfo {
   uint64_t seed;
@@ -64,27 +84,10 @@ struct TcParams {
   int k;
   int bpad;
   int stages;
-  int nbuf;  // bias tiles in shared memory (2: drain of t+1 overlaps t)
   int tiles_total;
   int n_chunks;
-  uint32_t u_off, bias_off, rows_off, bar_off;
+  uint32_t u_off, tile_off, stage_off, rows_off, bar_off;
 };
-
-// Running state of one (lane, request) over the lane's vocab entries:
-//   m    max of the scaled logits s seen (-inf if none);
-//   sum  sum of exp(s - m);
-//   key  the best candidate so far, relative to m: exp(s - m) / E for a
-//        sampled request (exponential race: the largest exp(s) / E is the
-//        largest s - log E = s + g), s itself for a greedy request;
-//   idx  its vocab index (kNoIndex while nothing has won).
-struct LaneStat {
-  float m, sum, key;
-  int idx;
-};
-
-__device__ __forceinline__ void named_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -92,122 +95,164 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+__device__ __forceinline__ void named_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Running state of one request in the compute warp that owns it:
+//   sum        per lane: sum of exp(s - best) over the lane's entries;
+//   best, idx  the same in every lane: the largest decision score so far
+//              (s + g for a sampled request, s for a greedy one) and its
+//              lowest vocab index (kNoIndex while nothing has won).
+struct RowState {
+  float sum, best;
+  int idx;
+};
+
+// The constant of the candidate test: 32 + 2^-11 - best log2(e)
+// (+inf while nothing has won, which admits every finite entry).
+__device__ __forceinline__ float thr_const(float best) {
+  return fmaf(-best, kLog2e, 32.0f + kThrSlack);
+}
+
+// 2^(32 + slack) exp(s - best).  A sampled entry wins only if s + g > best
+// with g = -log E, E = -log(1 - w) increasing in w = (x + 0.5) 2^-32, i.e.
+// only if w < 1 - exp(-(s - best)) <= exp(s - best).  The test
+// (float)x < this value is therefore conservative: the slack covers the
+// approximate exp2, the rounding of x and the error of the float32 score,
+// and entries that pass are decided exactly.
+__device__ __forceinline__ float test_value(float s, float tc) {
+  return ex2_approx(fmaf(s, kLog2e, tc));
+}
+
+// The exact decision score of a sampled entry, out of line so that it runs
+// only for the entries that pass the test.
+__device__ __noinline__ float exact_score(float s, uint32_t x) {
+  return __fadd_rn(s, -logf(exponential_from_word(x)));
+}
+
+__device__ __forceinline__ float pick4(const float (&a)[4], int e) {
+  return e == 0 ? a[0] : e == 1 ? a[1] : e == 2 ? a[2] : a[3];
+}
+
+// Scaled logit: the float32 IEEE quotient l / T; division by 1 is exact.
+template <bool kUnitT>
 __device__ __forceinline__ float scale(float l, float T) {
-  return T == 1.0f ? l : __fdiv_rn(l, T);
+  return kUnitT ? l : __fdiv_rn(l, T);
 }
 
-// Folds the four candidates v..v+3 (s[e] = -inf past V) into st.  E is the
-// exponential variate of each candidate (unused for greedy requests).
-template <bool kGreedy>
-__device__ __forceinline__ void fold4(LaneStat& st, const float s[4],
-                                      const float E[4], int v) {
-  const float m4 = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-  const float mn = fmaxf(st.m, m4);
-  if (mn > st.m) {  // a new running max: rescale what is kept relative to m
-    const float f = ex2_approx((st.m - mn) * kLog2e);
-    st.sum *= f;
-    if (!kGreedy) st.key *= f;
-    st.m = mn;
-  }
-  if (mn != -INFINITY) {
-    const float nml = -mn * kLog2e;
+// tcgen05.ld of four consecutive columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r0, r1, r2, r3;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(taddr)
+               : "memory");
+  v[0] = __uint_as_float(r0);
+  v[1] = __uint_as_float(r1);
+  v[2] = __uint_as_float(r2);
+  v[3] = __uint_as_float(r3);
+}
+
+// Keeps the better of st and the warp's candidates (cb, ci): a butterfly
+// with the usual order (larger score, then lower index).
+__device__ __forceinline__ void warp_take_best(RowState& st, float cb, int ci) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float ee = ex2_approx(fmaf(s[e], kLog2e, nml));
-      st.sum += ee;
-      const float key = kGreedy ? s[e] : __fdividef(ee, E[e]);
-      const bool win = key > st.key;  // strict: the lower index keeps a tie
-      st.key = win ? key : st.key;
-      st.idx = win ? v + e : st.idx;
+  for (int mask = 16; mask > 0; mask >>= 1) {
+    const float ob = __shfl_xor_sync(0xffffffffu, cb, mask);
+    const int oi = __shfl_xor_sync(0xffffffffu, ci, mask);
+    if (!better(cb, ci, ob, oi)) {
+      cb = ob;
+      ci = oi;
     }
-  } else if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3])) {
-    st.sum = __int_as_float(0x7fc00000);
+  }
+  if (ci != kNoIndex && better(cb, ci, st.best, st.idx)) {
+    st.best = cb;
+    st.idx = ci;
   }
 }
 
-// One request's four vocab entries v..v+3 of the tile: biased logits (written
-// when `store`), scaled logits, noise, and the fold into the lane state.
-__device__ __forceinline__ void process_row(const RowInfo& ri, size_t row,
-                                            const float4 bias, const float x[4],
-                                            bool valid, bool store, int v,
-                                            LaneStat& st, const DraftArgs& a,
-                                            int k, float T) {
-  float l[4], s[4];
-  l[0] = ri.pad ? bias.x : __fadd_rn(x[0], bias.x);
-  l[1] = ri.pad ? bias.y : __fadd_rn(x[1], bias.y);
-  l[2] = ri.pad ? bias.z : __fadd_rn(x[2], bias.z);
-  l[3] = ri.pad ? bias.w : __fadd_rn(x[3], bias.w);
-  if (valid && store)
-    __stcs(reinterpret_cast<float4*>(a.logits + row * a.V + v),
-           make_float4(l[0], l[1], l[2], l[3]));
+// Four entries v..v+3 of one request (biased logits l from shared memory):
+// scaled logits, the decision, and the sum-exp.
+template <bool kUnitT>
+__device__ __forceinline__ void process4(const RowInfo& ri, const float4 l4,
+                                         bool valid, int v, RowState& st,
+                                         int k, float T) {
+  float s[4];
+  s[0] = valid ? scale<kUnitT>(l4.x, T) : -INFINITY;
+  s[1] = valid ? scale<kUnitT>(l4.y, T) : -INFINITY;
+  s[2] = valid ? scale<kUnitT>(l4.z, T) : -INFINITY;
+  s[3] = valid ? scale<kUnitT>(l4.w, T) : -INFINITY;
+  const uint4 w = noise_block(ri.seed, ri.offset, k, kNoiseDraft, (uint32_t)v >> 2);
+  float tc = thr_const(st.best);
+  float f[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) s[e] = valid ? scale(l[e], T) : -INFINITY;
+  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+  uint32_t cand;
   if (ri.greedy) {
-    const float E[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-    fold4<true>(st, s, E, v);
+    cand = (s[0] > st.best ? 1u : 0u) | (s[1] > st.best ? 2u : 0u) |
+           (s[2] > st.best ? 4u : 0u) | (s[3] > st.best ? 8u : 0u);
   } else {
-    const uint4 w = noise_block(ri.seed, ri.offset, k, kNoiseDraft,
-                                (uint32_t)v >> 2);
-    float E[4];
-    E[0] = exponential_from_word(w.x);
-    E[1] = exponential_from_word(w.y);
-    E[2] = exponential_from_word(w.z);
-    E[3] = exponential_from_word(w.w);
-    fold4<false>(st, s, E, v);
+    cand = (__uint2float_rz(w.x) < f[0] ? 1u : 0u) |
+           (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
+           (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
+           (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
   }
-}
-
-template <typename BT>
-__device__ __forceinline__ void load_base4(const BT* p, float out[4]) {
-  if constexpr (sizeof(BT) == 4) {
-    const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
-    out[0] = x.x; out[1] = x.y; out[2] = x.z; out[3] = x.w;
-  } else {
-    const uint2 x = __ldcs(reinterpret_cast<const uint2*>(p));
-    out[0] = __uint_as_float(x.x << 16);
-    out[1] = __uint_as_float(x.x & 0xffff0000u);
-    out[2] = __uint_as_float(x.y << 16);
-    out[3] = __uint_as_float(x.y & 0xffff0000u);
-  }
-}
-
-template <int kN>
-__device__ __forceinline__ void tmem_ld4x(uint32_t taddr, float (&v)[4 * kN],
-                                          int n_valid) {
+  if (__any_sync(0xffffffffu, cand != 0u)) {
+    float cb = -INFINITY;
+    int ci = kNoIndex;
+    while (cand) {
+      const int e = __ffs(cand) - 1;
+      cand &= cand - 1u;
+      const float se = pick4(s, e);
+      const float sc = ri.greedy ? se : exact_score(se, word_of(w, e));
+      if (sc > cb) {  // e ascending: strict keeps the lower index
+        cb = sc;
+        ci = v + e;
+      }
+    }
+    const float old_best = st.best;
+    warp_take_best(st, cb, ci);
+    if (st.best != old_best) {  // new reference for the sum (uniform)
+      st.sum *= ex2_approx((old_best - st.best) * kLog2e);
+      tc = thr_const(st.best);
 #pragma unroll
-  for (int i = 0; i < kN; ++i) {
-    if (i < n_valid) {
-      uint32_t r0, r1, r2, r3;
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-          : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-          : "r"(taddr + 4u * i)
-          : "memory");
-      v[4 * i] = __uint_as_float(r0);
-      v[4 * i + 1] = __uint_as_float(r1);
-      v[4 * i + 2] = __uint_as_float(r2);
-      v[4 * i + 3] = __uint_as_float(r3);
+      for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
     }
   }
+  if (st.best == -INFINITY) {  // nothing has won: only NaN poisons the sum
+    if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3]))
+      st.sum = __int_as_float(0x7fc00000);
+  } else {
+    st.sum = fmaf(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
+                  kSumScale, st.sum);
+  }
 }
 
-template <typename BT>
+template <typename BT, bool kUnitT>
 __global__ void __launch_bounds__(kThreads, 1)
 position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
+                   const __grid_constant__ CUtensorMap base_map,
+                   const __grid_constant__ CUtensorMap out_map,
                    const __grid_constant__ TcParams P) {
+  constexpr bool kStaged = sizeof(BT) == 2;  // bf16 logits: via a staging tile
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
   uint8_t* ring = smem;
   uint8_t* u_s = smem + P.u_off;
-  float* bias_s = reinterpret_cast<float*>(smem + P.bias_off);
+  float* tiles = reinterpret_cast<float*>(smem + P.tile_off);
+  const BT* stage = reinterpret_cast<const BT*>(smem + P.stage_off);
   RowInfo* rows = reinterpret_cast<RowInfo*>(smem + P.rows_off);
   const int S = P.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.bar_off);
   uint64_t* empty = full + S;
   uint64_t* acc_full = empty + S;
   uint64_t* acc_empty = acc_full + 2;
-  uint64_t* mma_done = acc_empty + 2;
+  uint64_t* base_full = acc_empty + 2;
+  uint64_t* tile_free = base_full + 2;
+  uint64_t* stage_free = tile_free + 2;
+  uint64_t* mma_done = stage_free + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
@@ -218,6 +263,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   const int t_end = (int)((long long)(chunk + 1) * P.tiles_total / P.n_chunks);
   const int n_tiles = t_end - t_begin;
   const int kchunks = a.r / kKChunk;
+  const int tile_floats = P.bpad * kTileV;
 
   auto fail = [&](int code) {
     *abort_flag = 1;
@@ -233,49 +279,56 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
       mbar_init(&acc_empty[i], kComputeThreads);
+      mbar_init(&base_full[i], 1);
+      mbar_init(&tile_free[i], kComputeThreads);
     }
+    mbar_init(stage_free, kComputeThreads);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&wb_map);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&wb_map);
+    prefetch_tmap(&base_map);
+    prefetch_tmap(&out_map);
+  }
   if (warp == 1) {
     tmem_alloc(tmem_holder, kTmemCols);
     tmem_relinquish();
   }
   if (warp >= 2) {
-    // u_b = U[d_{k-1}(b)], stored r-major with the 128-byte swizzle: row n of
-    // r-chunk c at c*(bpad*128) + n*128, 16-byte piece p at (p ^ (n & 7)).
+    // u row b = U[d_{k-1}(b)], stored r-major with the 128-byte swizzle: row
+    // b of r-chunk c at c*(bpad*128) + b*128, 16-byte piece p at (p ^ (b & 7))
     const int ct = threadIdx.x - 64;
     const int pieces = a.r / 8;
     const uint16_t* U = static_cast<const uint16_t*>(a.U);
     for (int i = ct; i < P.bpad * pieces; i += kComputeThreads) {
-      const int n = i / pieces, piece = i - n * pieces;
+      const int b = i / pieces, piece = i - b * pieces;
       const int c = piece >> 3, p = piece & 7;
       uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (n < a.B) {
-        int prev = (P.k == 0) ? a.d0[n] : a.tokens[(size_t)n * a.K + (P.k - 1)];
+      if (b < a.B) {
+        int prev = (P.k == 0) ? a.d0[b] : a.tokens[(size_t)b * a.K + (P.k - 1)];
         if ((unsigned)prev >= (unsigned)a.V) {
           if (piece == 0) a.control[0] = kDevErrBadToken;
           prev = 0;
         }
         val = __ldg(reinterpret_cast<const uint4*>(U + (size_t)prev * a.r) + piece);
       }
-      *reinterpret_cast<uint4*>(u_s + (size_t)c * (P.bpad * 128) + n * 128 +
-                                ((p ^ (n & 7)) << 4)) = val;
+      *reinterpret_cast<uint4*>(u_s + (size_t)c * (P.bpad * 128) + b * 128 +
+                                ((p ^ (b & 7)) << 4)) = val;
     }
-    for (int n = ct; n < P.bpad; n += kComputeThreads) {
+    for (int b = ct; b < P.bpad; b += kComputeThreads) {
       RowInfo ri;
-      if (n < a.B) {
-        ri.seed = a.seed[n];
-        ri.offset = a.offset[n];
-        ri.pad = a.pad_row != nullptr && a.pad_row[n] != 0;
-        ri.greedy = a.greedy != nullptr && a.greedy[n] != 0;
+      if (b < a.B) {
+        ri.seed = a.seed[b];
+        ri.offset = a.offset[b];
+        ri.pad = a.pad_row != nullptr && a.pad_row[b] != 0;
+        ri.greedy = a.greedy != nullptr && a.greedy[b] != 0;
       } else {
         ri.seed = ri.offset = 0;
         ri.pad = ri.greedy = 0;
       }
-      rows[n] = ri;
+      rows[b] = ri;
     }
     fence_proxy_async_smem();
   }
@@ -285,8 +338,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // -------------------------------------------------- Wb producer
       int g = 0;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t) {
         const int v0 = (t_begin + t) * kTileV;
@@ -303,12 +356,40 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           tma_load_2d(dst + kBoxBytes, &wb_map, &full[s], v0 + 64, kc * kKChunk);
         }
       }
-      // every issued load lands before the CTA may exit: wait for the last
-      // phase of each stage that was used (bounded; only matters on abort)
-      if (*abort_flag) {
+      if (*abort_flag) {  // let every issued load land (bounded)
         for (int s = 0; s < S && s < g; ++s) {
           const int last = g - 1 - ((g - 1 - s) % S);
           mbar_wait(&full[s], (uint32_t)(last / S) & 1u, kSpin >> 4);
+        }
+      }
+    } else if (lane == 1) {
+      // ----------------------------------------- drafter-logit producer
+      const uint32_t bytes = (uint32_t)(tile_floats * (int)sizeof(BT));
+      int issued = 0;
+      for (int t = 0; t < n_tiles && !*abort_flag; ++t, ++issued) {
+        const int v0 = (t_begin + t) * kTileV;
+        if (kStaged) {
+          if (!mbar_wait(stage_free, ((uint32_t)t & 1u) ^ 1u, kSpin)) {
+            fail(kDevErrTimeout);
+            break;
+          }
+          mbar_arrive_expect_tx(&base_full[0], bytes);
+          tma_load_2d(const_cast<BT*>(stage), &base_map, &base_full[0], v0, 0);
+        } else {
+          const int buf = t & 1;
+          if (!mbar_wait(&tile_free[buf], ((uint32_t)(t >> 1) & 1u) ^ 1u, kSpin)) {
+            fail(kDevErrTimeout);
+            break;
+          }
+          mbar_arrive_expect_tx(&base_full[buf], bytes);
+          tma_load_2d(tiles + (size_t)buf * tile_floats, &base_map, &base_full[buf], v0, 0);
+        }
+      }
+      if (*abort_flag) {  // let every issued load land (bounded)
+        for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t) {
+          const int buf = kStaged ? 0 : (t & 1);
+          const uint32_t ph = kStaged ? ((uint32_t)t & 1u) : ((uint32_t)(t >> 1) & 1u);
+          mbar_wait(&base_full[buf], ph, kSpin >> 4);
         }
       }
     }
@@ -364,97 +445,102 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   } else {
     // ----------------------------------------------------------- compute
     const int cw = warp - 2;
-    const int quarter = warp & 3;        // TMEM lanes this warp may access
-    const int col_group = cw >> 2;       // which quarter of the columns
-    const int cols = P.bpad / 4;         // columns drained by this warp
-    const int col0 = col_group * cols;
-    const BT* base = static_cast<const BT*>(a.base);
+    const int q = warp & 3;                  // TMEM lane quarter
+    const int gcols = P.bpad / 4;            // drained columns (requests)
+    const int col0 = (cw >> 2) * gcols;
+    const int m = 32 * q + lane;             // drained vocab row of the tile
+    const int rpw = P.bpad / kComputeWarps;  // requests per warp
+    const bool storer = cw == 0 && lane == 0;
     const float T = a.T;
     const int V = a.V;
-    LaneStat st[kMaxRowsPerWarp];
+    RowState st[kMaxRows];
 #pragma unroll
-    for (int i = 0; i < kMaxRowsPerWarp; ++i) {
-      st[i].m = -INFINITY;
+    for (int i = 0; i < kMaxRows; ++i) {
       st[i].sum = 0.0f;
-      st[i].key = 0.0f;
+      st[i].best = -INFINITY;  // nothing to beat yet
       st[i].idx = kNoIndex;
-    }
-#pragma unroll
-    for (int i = 0; i < kMaxRowsPerWarp; ++i) {
-      const int b = cw + kComputeWarps * i;
-      if (b < a.B && rows[b].greedy) st[i].key = -INFINITY;
     }
 
     for (int t = 0; t < n_tiles; ++t) {
-      const int acc = t & 1;
-      const uint32_t aph = (uint32_t)(t >> 1) & 1u;
-      float* bias_t = bias_s + (P.nbuf == 2 ? acc : 0) * (P.bpad * kTileV);
-      // drain: lanes quarter*32.., columns col0..col0+cols of the accumulator
-      bool ok = !*abort_flag && mbar_wait(&acc_full[acc], aph, kSpin);
+      const int buf = t & 1;
+      const uint32_t ph = (uint32_t)(t >> 1) & 1u;
+      const int v0 = (t_begin + t) * kTileV;
+      float* tile = tiles + (size_t)buf * tile_floats;
+      // drain: l = base + bias for this warp's (vocab row m, request) block
+      bool ok = !*abort_flag &&
+                mbar_wait(kStaged ? &base_full[0] : &base_full[buf],
+                          kStaged ? ((uint32_t)t & 1u) : ph, kSpin) &&
+                mbar_wait(&acc_full[buf], ph, kSpin);
       ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
       if (ok) {
         tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) +
-                               (uint32_t)acc * kAccCols + (uint32_t)col0;
-        float vals[kMaxBpad / 4];
-        tmem_ld4x<kMaxBpad / 16>(taddr, vals, cols / 4);
-        tmem_ld_wait();
-        const int m = quarter * 32 + lane;
+        const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
+                               (uint32_t)buf * kAccCols + (uint32_t)col0;
+        for (int c0 = 0; c0 < gcols; c0 += 4) {
+          float bias[4];
+          tmem_ld4(taddr + (uint32_t)c0, bias);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < kMaxBpad / 4; ++i)
-          if (i < cols) bias_t[(col0 + i) * kTileV + m] = vals[i];
+          for (int i = 0; i < 4; ++i) {
+            const int b = col0 + c0 + i;
+            if (b < a.B) {
+              float x;
+              if (kStaged)
+                x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(
+                                        stage)[b * kTileV + m] << 16);
+              else
+                x = tile[b * kTileV + m];
+              tile[b * kTileV + m] = rows[b].pad ? bias[i] : __fadd_rn(x, bias[i]);
+            }
+          }
+        }
         tc_fence_before();
       } else if (!*abort_flag) {
         fail(kDevErrTimeout);
       }
-      mbar_arrive(&acc_empty[acc]);
-      // bias tile complete (and, with two tiles, the other one is free again:
-      // every warp finished computing on it before arriving here)
-      named_sync(1, kComputeThreads);
+      mbar_arrive(&acc_empty[buf]);
+      if (kStaged) mbar_arrive(stage_free);
+      fence_proxy_async_smem();  // the tile store reads these writes
+      named_sync(1, kComputeThreads);  // the tile holds the biased logits
+      if (storer && !*abort_flag) {
+        tma_store_2d(&out_map, tile, v0, 0);
+        bulk_commit();
+      }
       if (!*abort_flag) {
-        const int v = (t_begin + t) * kTileV + 4 * lane;
+        const int v = v0 + 4 * lane;
         const bool valid = v < V;  // V % 8 == 0: v..v+3 all in range
 #pragma unroll
-        for (int i = 0; i < kMaxRowsPerWarp; ++i) {
+        for (int i = 0; i < kMaxRows; ++i) {
+          if (i >= rpw) break;
           const int b = cw + kComputeWarps * i;
           if (b >= a.B) break;
-          const RowInfo ri = rows[b];
-          const float4 bias =
-              *reinterpret_cast<const float4*>(bias_t + b * kTileV + 4 * lane);
-          const size_t row = (size_t)b * a.K + P.k;
-          float x[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-          if (!ri.pad && valid) load_base4<BT>(base + row * V + v, x);
-          process_row(ri, row, bias, x, valid, true, v, st[i], a, P.k, T);
+          const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
+          process4<kUnitT>(rows[b], l4, valid, v, st[i], P.k, T);
         }
       }
-      if (P.nbuf == 1) named_sync(2, kComputeThreads);  // bias tile consumed
+      if (storer) bulk_wait_read_all();  // the store has read the tile
+      mbar_arrive(&tile_free[buf]);
     }
-    // chunk statistics: the lane winner's log-domain score s + g, then a
-    // butterfly over the warp
+    if (storer) bulk_wait_all();
+    // chunk statistics: best score and index (already warp-wide), the
+    // lanes' sums (same reference) added by a butterfly
 #pragma unroll
-    for (int i = 0; i < kMaxRowsPerWarp; ++i) {
+    for (int i = 0; i < kMaxRows; ++i) {
+      if (i >= rpw) break;
       const int b = cw + kComputeWarps * i;
       if (b >= a.B) break;
-      const RowInfo ri = rows[b];
-      ChunkStat cs;
-      cs.idx = st[i].idx;
-      cs.m = st[i].m;
-      cs.s = st[i].sum;
-      cs.best = -INFINITY;
-      if (cs.idx != kNoIndex) {
-        if (ri.greedy) {
-          cs.best = st[i].key;
-        } else {
-          const size_t row = (size_t)b * a.K + P.k;
-          const float s_best = scale(a.logits[row * V + cs.idx], T);
-          const uint4 w = noise_block(ri.seed, ri.offset, P.k, kNoiseDraft,
-                                      (uint32_t)cs.idx >> 2);
-          cs.best = __fadd_rn(
-              s_best, -logf(exponential_from_word(word_of(w, cs.idx & 3))));
-        }
+      float sum = st[i].sum;
+#pragma unroll
+      for (int mask = 16; mask > 0; mask >>= 1)
+        sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, mask));
+      if (lane == 0) {
+        ChunkStat cs;
+        cs.best = st[i].best;
+        cs.idx = st[i].idx;
+        cs.m = st[i].best;  // the reference of the sum (-inf: nothing won)
+        cs.s = sum;
+        a.stats[(size_t)b * kMaxChunks + chunk] = cs;
       }
-      const ChunkStat red = warp_reduce_stat(cs);
-      if (lane == 0) a.stats[(size_t)b * kMaxChunks + chunk] = red;
     }
   }
 
@@ -483,83 +569,122 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct Layout {
-  int bpad, stages, nbuf;
-  uint32_t u_off, bias_off, rows_off, bar_off;
+  int bpad, stages;
+  uint32_t u_off, tile_off, stage_off, rows_off, bar_off;
   size_t smem;
 };
 
-// Shared memory: the Wb ring, u, one or two bias tiles, row info, barriers.
-// Two bias tiles are used when at least four ring stages still fit.
-Layout make_layout(int B, int r) {
+// Shared memory: the Wb ring, u, two float32 tile buffers [bpad][128], a
+// bf16 staging tile when the drafter logits are bf16, row info, barriers.
+Layout make_layout(int B, int r, int base_elt) {
   Layout L;
   L.bpad = (B + 15) / 16 * 16;
   const size_t u = (size_t)L.bpad * r * 2;
-  const size_t bias = (size_t)L.bpad * kTileV * 4;
+  const size_t tiles = 2 * (size_t)L.bpad * kTileV * 4;
+  const size_t stage = base_elt == 2 ? (size_t)L.bpad * kTileV * 2 : 0;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowInfo), 16);
-  const size_t bars_max = (2 * kMaxStages + 5) * 8 + 16;
-  for (L.nbuf = 2; L.nbuf >= 1; --L.nbuf) {
-    const size_t fixed = u + L.nbuf * bias + rows + bars_max + 1024;
-    L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
-    if (L.stages > kMaxStages) L.stages = kMaxStages;
-    if (L.stages >= 4 || L.nbuf == 1) break;
-  }
+  const size_t bars = (2 * kMaxStages + 10) * 8 + 16;
+  const size_t fixed = u + tiles + stage + rows + bars + 1024;
+  L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
+  if (L.stages > kMaxStages) L.stages = kMaxStages;
   L.u_off = (uint32_t)((size_t)L.stages * kStageBytes);
-  L.bias_off = (uint32_t)(L.u_off + u);
-  L.rows_off = (uint32_t)(L.bias_off + L.nbuf * bias);
+  L.tile_off = (uint32_t)(L.u_off + u);
+  L.stage_off = (uint32_t)(L.tile_off + tiles);
+  L.rows_off = (uint32_t)(L.stage_off + stage);
   L.bar_off = (uint32_t)(L.rows_off + rows);
-  L.smem = L.bar_off + (2 * L.stages + 5) * 8 + 16 + 1024;
+  L.smem = L.bar_off + bars + 1024;
   return L;
+}
+
+// A [rows, V] view of one position of a [B, K, V] tensor: dims {V, B},
+// row stride K*V elements, box {128, bpad}, no swizzle.
+CUresult encode_position_map(CUtensorMap* map, CUtensorMapDataType dt,
+                             const void* base, int elt, int B, int K, int V,
+                             int k, int bpad) {
+  const cuuint64_t dims[2] = {(cuuint64_t)V, (cuuint64_t)B};
+  const cuuint64_t strides[1] = {(cuuint64_t)K * V * elt};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileV, (cuuint32_t)bpad};
+  const cuuint32_t estr[2] = {1, 1};
+  void* addr = const_cast<char*>(static_cast<const char*>(base)) +
+               (size_t)k * V * elt;
+  return encode_fn()(map, dt, 2, addr, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+template <typename BT, bool kUnitT>
+cudaError_t launch_typed(const CUtensorMap& wb, const CUtensorMap& bm,
+                         const CUtensorMap& om, const TcParams& P, size_t smem,
+                         int n_chunks, cudaStream_t stream) {
+  auto kern = position_tc_kernel<BT, kUnitT>;
+  cudaError_t err = cudaFuncSetAttribute(
+      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  kern<<<n_chunks, kThreads, smem, stream>>>(wb, bm, om, P);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 bool position_tc_supported(const DraftArgs& a) {
+  const int elt = a.base_dtype == DSPARK_F32 ? 4 : 2;
   return a.w_dtype == DSPARK_BF16 && a.r % kKChunk == 0 && a.r <= 256 &&
-         a.V % 8 == 0 && a.B <= kMaxBpad && make_layout(a.B, a.r).stages >= 2 &&
+         a.V % 8 == 0 && a.B <= kMaxBpad &&
+         make_layout(a.B, a.r, elt).stages >= kMinStages &&
          encode_fn() != nullptr;
 }
 
+// CTAs of the tensor-core kernel: one per SM, at most one per vocab tile.
 int position_tc_chunks(int V, int sm_count) {
   const int tiles = (V + kTileV - 1) / kTileV;
-  return tiles < sm_count ? tiles : sm_count;
+  int n = tiles < sm_count ? tiles : sm_count;
+  return n < kMaxChunks ? n : kMaxChunks;
 }
 
 cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
                                cudaStream_t stream) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
-  if (!encode) return cudaErrorNotSupported;
-  CUtensorMap map;
-  const cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
-  const cuuint64_t strides[1] = {(cuuint64_t)a.V * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kKChunk};
-  const cuuint32_t estr[2] = {1, 1};
-  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                       const_cast<void*>(a.Wb), dims, strides, box, estr,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  const Layout L = make_layout(a.B, a.r);
+  if (!encode_fn()) return cudaErrorNotSupported;
+  const int elt = a.base_dtype == DSPARK_F32 ? 4 : 2;
+  const Layout L = make_layout(a.B, a.r, elt);
+  CUtensorMap wb, bm, om;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.V, (cuuint64_t)a.r};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.V * 2};
+    const cuuint32_t box[2] = {64, (cuuint32_t)kKChunk};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode_fn()(&wb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(a.Wb), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  if (encode_position_map(&bm,
+                          elt == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                          a.base, elt, a.B, a.K, a.V, k, L.bpad) != CUDA_SUCCESS ||
+      encode_position_map(&om, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, a.logits, 4,
+                          a.B, a.K, a.V, k, L.bpad) != CUDA_SUCCESS)
+    return cudaErrorInvalidValue;
   TcParams P;
   P.a = a;
   P.k = k;
   P.bpad = L.bpad;
   P.stages = L.stages;
-  P.nbuf = L.nbuf;
   P.tiles_total = (a.V + kTileV - 1) / kTileV;
   P.n_chunks = n_chunks;
   P.u_off = L.u_off;
-  P.bias_off = L.bias_off;
+  P.tile_off = L.tile_off;
+  P.stage_off = L.stage_off;
   P.rows_off = L.rows_off;
   P.bar_off = L.bar_off;
-  auto kern = a.base_dtype == DSPARK_F32 ? position_tc_kernel<float>
-                                         : position_tc_kernel<uint16_t>;
-  cudaError_t err = cudaFuncSetAttribute(
-      kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
-  if (err != cudaSuccess) return err;
-  kern<<<n_chunks, kThreads, L.smem, stream>>>(map, P);
-  return cudaGetLastError();
+  const bool unit = a.T == 1.0f;
+  if (elt == 4)
+    return unit ? launch_typed<float, true>(wb, bm, om, P, L.smem, n_chunks, stream)
+                : launch_typed<float, false>(wb, bm, om, P, L.smem, n_chunks, stream);
+  return unit ? launch_typed<uint16_t, true>(wb, bm, om, P, L.smem, n_chunks, stream)
+              : launch_typed<uint16_t, false>(wb, bm, om, P, L.smem, n_chunks, stream);
 }
 
 }  // namespace dspark
