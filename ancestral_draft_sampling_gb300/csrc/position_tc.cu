@@ -154,22 +154,51 @@ __device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
   v[3] = __uint_as_float(r3);
 }
 
-// Keeps the better of st and the warp's candidates (cb, ci): a butterfly
-// with the usual order (larger score, then lower index).
+// Float32 -> uint32 map that preserves order (for finite and infinite
+// values): flip every bit of negatives, set the sign bit of the others.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered_bits(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Keeps the better of st and the warp's candidates (cb, ci): the largest
+// score by a max-reduction over order-preserving bits, then the lowest index
+// among the lanes that hold it by a min-reduction.  Lanes without a
+// candidate offer key 0 (below every score, -inf included).
 __device__ __forceinline__ void warp_take_best(RowState& st, float cb, int ci) {
-#pragma unroll
-  for (int mask = 16; mask > 0; mask >>= 1) {
-    const float ob = __shfl_xor_sync(0xffffffffu, cb, mask);
-    const int oi = __shfl_xor_sync(0xffffffffu, ci, mask);
-    if (!better(cb, ci, ob, oi)) {
-      cb = ob;
-      ci = oi;
+  const uint32_t key = ci == kNoIndex ? 0u : ordered_bits(cb);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  if (kmax == 0u) return;
+  const uint32_t imin = __reduce_min_sync(
+      0xffffffffu, key == kmax ? (uint32_t)ci : 0xffffffffu);
+  const float wb = from_ordered_bits(kmax);
+  if (better(wb, (int)imin, st.best, st.idx)) {
+    st.best = wb;
+    st.idx = (int)imin;
+  }
+}
+
+// Exact scores of the entries in `cand` (bit e = entry v+e), merged into st.
+__device__ __forceinline__ void decide(RowState& st, uint32_t cand,
+                                       const float (&s)[4], const uint4 w,
+                                       bool greedy, int v) {
+  float cb = -INFINITY;
+  int ci = kNoIndex;
+  while (cand) {
+    const int e = __ffs(cand) - 1;
+    cand &= cand - 1u;
+    const float se = pick4(s, e);
+    const float sc = greedy ? se : exact_score(se, word_of(w, e));
+    if (sc > cb) {  // e ascending: strict keeps the lower index
+      cb = sc;
+      ci = v + e;
     }
   }
-  if (ci != kNoIndex && better(cb, ci, st.best, st.idx)) {
-    st.best = cb;
-    st.idx = ci;
-  }
+  warp_take_best(st, cb, ci);
 }
 
 // Four entries v..v+3 of one request (biased logits l from shared memory):
@@ -184,41 +213,52 @@ __device__ __forceinline__ void process4(const RowInfo& ri, const float4 l4,
   s[2] = valid ? scale<kUnitT>(l4.z, T) : -INFINITY;
   s[3] = valid ? scale<kUnitT>(l4.w, T) : -INFINITY;
   const uint4 w = noise_block(ri.seed, ri.offset, k, kNoiseDraft, (uint32_t)v >> 2);
-  float tc = thr_const(st.best);
+  const bool greedy = ri.greedy != 0;
   float f[4];
+  const float old_best = st.best;
+  if (old_best == -INFINITY) {
+    // Nothing has won yet (the first tile of the chunk): decide each lane's
+    // largest entry exactly, then test the others against that best.
+    uint32_t first = 0;
+    float top = -INFINITY;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
-  uint32_t cand;
-  if (ri.greedy) {
-    cand = (s[0] > st.best ? 1u : 0u) | (s[1] > st.best ? 2u : 0u) |
-           (s[2] > st.best ? 4u : 0u) | (s[3] > st.best ? 8u : 0u);
-  } else {
-    cand = (__uint2float_rz(w.x) < f[0] ? 1u : 0u) |
-           (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
-           (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
-           (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
-  }
-  if (__any_sync(0xffffffffu, cand != 0u)) {
-    float cb = -INFINITY;
-    int ci = kNoIndex;
-    while (cand) {
-      const int e = __ffs(cand) - 1;
-      cand &= cand - 1u;
-      const float se = pick4(s, e);
-      const float sc = ri.greedy ? se : exact_score(se, word_of(w, e));
-      if (sc > cb) {  // e ascending: strict keeps the lower index
-        cb = sc;
-        ci = v + e;
+    for (int e = 0; e < 4; ++e)
+      if (s[e] > top) {
+        top = s[e];
+        first = 1u << e;
       }
-    }
-    const float old_best = st.best;
-    warp_take_best(st, cb, ci);
-    if (st.best != old_best) {  // new reference for the sum (uniform)
-      st.sum *= ex2_approx((old_best - st.best) * kLog2e);
-      tc = thr_const(st.best);
+    if (__any_sync(0xffffffffu, first != 0u)) decide(st, first, s, w, greedy, v);
+    const float tc = thr_const(st.best);
+    uint32_t cand = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+    for (int e = 0; e < 4; ++e) {
+      f[e] = test_value(s[e], tc);
+      const bool c = greedy ? s[e] > st.best : __uint2float_rz(word_of(w, e)) < f[e];
+      cand |= (c ? 1u : 0u) << e;
     }
+    cand &= ~first;
+    if (__any_sync(0xffffffffu, cand != 0u)) decide(st, cand, s, w, greedy, v);
+  } else {
+    const float tc = thr_const(old_best);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+    uint32_t cand;
+    if (greedy) {
+      cand = (s[0] > old_best ? 1u : 0u) | (s[1] > old_best ? 2u : 0u) |
+             (s[2] > old_best ? 4u : 0u) | (s[3] > old_best ? 8u : 0u);
+    } else {
+      cand = (__uint2float_rz(w.x) < f[0] ? 1u : 0u) |
+             (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
+             (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
+             (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
+    }
+    if (__any_sync(0xffffffffu, cand != 0u)) decide(st, cand, s, w, greedy, v);
+  }
+  if (st.best != old_best) {  // a new reference for the sum (warp-uniform)
+    if (old_best != -INFINITY) st.sum *= ex2_approx((old_best - st.best) * kLog2e);
+    const float tc = thr_const(st.best);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
   }
   if (st.best == -INFINITY) {  // nothing has won: only NaN poisons the sum
     if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3]))
@@ -451,6 +491,10 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     const int m = 32 * q + lane;             // drained vocab row of the tile
     const int rpw = P.bpad / kComputeWarps;  // requests per warp
     const bool storer = cw == 0 && lane == 0;
+    // drained columns that hold requests (< B), and which are padding rows
+    const int nvalid = a.B - col0 < 0 ? 0 : (a.B - col0 < gcols ? a.B - col0 : gcols);
+    uint32_t padmask = 0;
+    for (int c = 0; c < nvalid; ++c) padmask |= (rows[col0 + c].pad ? 1u : 0u) << c;
     const float T = a.T;
     const int V = a.V;
     RowState st[kMaxRows];
@@ -476,23 +520,29 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
                                (uint32_t)buf * kAccCols + (uint32_t)col0;
-        for (int c0 = 0; c0 < gcols; c0 += 4) {
-          float bias[4];
-          tmem_ld4(taddr + (uint32_t)c0, bias);
-          tmem_ld_wait();
+        float bias[kMaxBpad / 4];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int b = col0 + c0 + i;
-            if (b < a.B) {
-              float x;
-              if (kStaged)
-                x = __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(
-                                        stage)[b * kTileV + m] << 16);
-              else
-                x = tile[b * kTileV + m];
-              tile[b * kTileV + m] = rows[b].pad ? bias[i] : __fadd_rn(x, bias[i]);
-            }
+        for (int c = 0; c < kMaxBpad / 4; c += 4)
+          if (c < gcols) {
+            float q4[4];
+            tmem_ld4(taddr + (uint32_t)c, q4);
+            bias[c] = q4[0];
+            bias[c + 1] = q4[1];
+            bias[c + 2] = q4[2];
+            bias[c + 3] = q4[3];
           }
+        tmem_ld_wait();
+        float* col = tile + col0 * kTileV + m;
+#pragma unroll
+        for (int c = 0; c < kMaxBpad / 4; ++c) {
+          if (c >= nvalid) break;
+          float x;
+          if (kStaged)
+            x = __uint_as_float(
+                (uint32_t)reinterpret_cast<const uint16_t*>(stage)[(col0 + c) * kTileV + m] << 16);
+          else
+            x = col[c * kTileV];
+          col[c * kTileV] = ((padmask >> c) & 1u) ? bias[c] : __fadd_rn(x, bias[c]);
         }
         tc_fence_before();
       } else if (!*abort_flag) {
