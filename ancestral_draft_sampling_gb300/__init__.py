@@ -15,7 +15,7 @@ from typing import Optional
 from . import _lib
 from ._lib import BF16, F32, DsparkError  # noqa: F401
 
-__all__ = ["draft_block", "draft_block_profile", "verify_standard", "noise_words", "workspace_bytes",
+__all__ = ["draft_block", "draft_block_noalloc", "draft_block_profile", "verify_standard", "noise_words", "workspace_bytes",
            "read_device_error", "DraftWorkspace", "DsparkError", "F32", "BF16",
            "version"]
 
@@ -103,6 +103,32 @@ def draft_block(base_logits, U, Wb, d0, seed, offset, T: float, *,
         _ptr(draft_probs), _ptr(workspace.buffer), workspace.nbytes,
         _stream(stream))
     _lib.check("dspark_draft_block", st)
+    return tokens, logits, draft_probs
+
+
+def draft_block_noalloc(base_logits, U, Wb, d0, seed, offset, T: float, *,
+                        greedy=None, pad_row=None, tokens=None, logits=None,
+                        draft_probs=None, stream=None):
+    """dspark_draft_block_noalloc: the draft block with library-owned scratch
+    instead of a caller-provided workspace (for callers that cannot allocate
+    device memory).  Outputs must be passed in; nothing is allocated here
+    either when they are."""
+    torch = _torch()
+    B, K, V = base_logits.shape
+    r = U.shape[1]
+    dev = base_logits.device
+    if tokens is None:
+        tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if logits is None:
+        logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if draft_probs is None:
+        draft_probs = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    st = _lib.load().dspark_draft_block_noalloc(
+        _ptr(base_logits), _dtype_code(base_logits), _ptr(U), _ptr(Wb),
+        _dtype_code(U), _ptr(d0), _ptr(seed), _ptr(offset), float(T),
+        _ptr(greedy), _ptr(pad_row), B, K, V, r, _ptr(tokens), _ptr(logits),
+        _ptr(draft_probs), _stream(stream))
+    _lib.check("dspark_draft_block_noalloc", st)
     return tokens, logits, draft_probs
 
 

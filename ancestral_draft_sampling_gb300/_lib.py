@@ -29,6 +29,7 @@ EXPORTED = (
     "dspark_draft_workspace_bytes",
     "dspark_draft_block",
     "dspark_draft_block_profile",
+    "dspark_draft_block_noalloc",
     "dspark_verify_standard",
     "dspark_noise_words",
     "dspark_read_device_error",
@@ -69,6 +70,10 @@ def load() -> ctypes.CDLL:
             P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
             P, ctypes.c_size_t, P, P, P]
         lib.dspark_draft_block_profile.restype = I
+        lib.dspark_draft_block_noalloc.argtypes = [
+            P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
+            P]
+        lib.dspark_draft_block_noalloc.restype = I
         lib.dspark_verify_standard.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
         lib.dspark_verify_standard.restype = I
         lib.dspark_noise_words.argtypes = [U64, U64, I, I, I, P, P, P]

@@ -11,6 +11,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 
 #include "dspark_common.cuh"
 
@@ -168,6 +169,33 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   return timed_launch(t, 2, stream, proposals_adapter, a, 0, 0);
 }
 
+// ---------------------------------------------------- allocation-free scratch
+// The scratch of dspark_draft_block_noalloc: one file-scope device array,
+// loaded with the library on every GPU that uses it and held until exit.
+constexpr size_t kNoallocScratchBytes = size_t(2) << 20;  // 2 MiB
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device.  The symbol
+// name is a host-side stand-in, never a device address, so it is resolved
+// once per device (with that device current) and cached.
+cudaError_t noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return cudaSuccess;
+}
+
 }  // namespace
 
 extern "C" {
@@ -244,6 +272,33 @@ dspark_status dspark_draft_block_profile(
   }
   for (int i = 0; i < created; ++i) cudaEventDestroy(t.ev[i]);
   return st;
+}
+
+dspark_status dspark_draft_block_noalloc(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, cudaStream_t stream) {
+  // host-side checks first, against a stand-in scratch address
+  DraftArgs a;
+  void* const stand_in = reinterpret_cast<void*>(uintptr_t(256));
+  dspark_status st = prepare_draft(
+      base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
+      pad_row, B, K, V, r, tokens, logits, draft_probs, stand_in,
+      kNoallocScratchBytes, a);
+  if (st != DSPARK_OK) return st;  // sizes past the scratch: WORKSPACE
+  void* scratch = nullptr;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return DSPARK_ERR_CUDA;
+  st = prepare_draft(base_logits, base_dtype, U, Wb, w_dtype, d0, seed,
+                     offset, T, greedy, pad_row, B, K, V, r, tokens, logits,
+                     draft_probs, scratch, kNoallocScratchBytes, a);
+  if (st != DSPARK_OK) return st;
+  // the scratch keeps the previous call's contents: only the device error
+  // word must start at zero (every other word is written before it is read)
+  if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
+  return run_block(a, stream, nullptr);
 }
 
 dspark_status dspark_verify_standard(const float* draft_probs,

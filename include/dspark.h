@@ -145,6 +145,38 @@ DSPARK_API dspark_status dspark_draft_block_profile(
     cudaStream_t stream);
 
 /*
+ * dspark_draft_block_noalloc -- dspark_draft_block for callers that cannot
+ * allocate device memory: code that is handed only its input and output
+ * buffers by a host runtime that owns all device memory (an inference
+ * server that sizes every allocation at start-up and forbids allocation
+ * afterwards), or that runs where cudaMalloc must not be called.  There is
+ * no counterpart in the pages; it is the same launch sequence as
+ * dspark_draft_block with the workspace replaced by library-owned scratch.
+ *
+ * Arguments and outputs are those of dspark_draft_block without
+ * `workspace` / `workspace_bytes`.  The scratch is one file-scope device
+ * array of DSPARK_NOALLOC_SCRATCH_BYTES bytes (2 MiB), held on every GPU
+ * that loads the library until the process exits; sizes whose workspace
+ * (dspark_draft_workspace_bytes) exceeds it are rejected with
+ * DSPARK_ERR_WORKSPACE before any launch (e.g. B <= 127 at K = 7).
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.  The first call on a device looks up the scratch's device
+ * address (with that device current); make that first call before any
+ * stream capture.  Every call on a device shares the one scratch array and
+ * it keeps the last call's contents (each call zeroes the device error word
+ * it starts with); calls that overlap on the GPU, from any stream or thread,
+ * race on it and must be serialised by the caller.  Device-side error codes
+ * of this variant stay in the scratch and are not reported.
+ */
+#define DSPARK_NOALLOC_SCRATCH_BYTES (2u << 20)
+DSPARK_API dspark_status dspark_draft_block_noalloc(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, cudaStream_t stream);
+
+/*
  * dspark_verify_standard -- standard token-level rejection sampling of the
  * drafts (PR #21, "2. Golden sampling semantics": the default rule), for B
  * requests.
