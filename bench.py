@@ -137,30 +137,29 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
-def kernel_source_hash():
+def source_hash(names):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ancestral_draft_sampling_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(kernel: str):
     """DRAM bytes per launch of `kernel` from the committed ncu summary, or
-    None when the kernel sources changed since the counters were taken."""
+    None when the kernel's sources changed since the counters were taken."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
-    except (OSError, ValueError):
+        ent = d[kernel]
+        if ent["source_hash"] != source_hash(ent["sources"]):
+            return None
+        return ent["dram_bytes_per_launch"]
+    except (OSError, ValueError, KeyError):
         return None
-    ent = d.get(kernel)
-    if not ent or ent.get("source_hash") != kernel_source_hash():
-        return None
-    return ent.get("dram_bytes_per_launch")
 
 
 # ------------------------------------------------------------ CPU oracle
