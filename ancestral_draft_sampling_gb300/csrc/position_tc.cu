@@ -72,12 +72,15 @@ constexpr float kThrSlack = 0x1p-11f;
 // 2^-(32 + 2^-11), rounded to float32 (relative error < 2^-24)
 constexpr float kSumScale = 2.3275186e-10f;
 
-struct RowInfo {
-  uint64_t seed;
-  uint64_t offset;
-  int pad;
-  int greedy;
+// Per-request constants in shared memory.  The Philox round keys of the
+// request's key (seed) are precomputed, so a noise block costs the ten
+// rounds' multiplies and XORs only.
+struct RowConst {
+  uint32_t rk[20];    // round r uses (rk[2r], rk[2r+1]) = key + r * (W0, W1)
+  uint32_t c1, c2, c3;  // counter words 1..3: k | stream << 16, offset lo, hi
+  uint32_t flags;     // bit 0: padding row, bit 1: greedy request
 };
+constexpr uint32_t kRowPad = 1u, kRowGreedy = 2u;
 
 struct TcParams {
   DraftArgs a;
@@ -123,12 +126,6 @@ __device__ __forceinline__ float thr_const(float best) {
 // and entries that pass are decided exactly.
 __device__ __forceinline__ float test_value(float s, float tc) {
   return ex2_approx(fmaf(s, kLog2e, tc));
-}
-
-// The exact decision score of a sampled entry, out of line so that it runs
-// only for the entries that pass the test.
-__device__ __noinline__ float exact_score(float s, uint32_t x) {
-  return __fadd_rn(s, -logf(exponential_from_word(x)));
 }
 
 __device__ __forceinline__ float pick4(const float (&a)[4], int e) {
@@ -182,17 +179,34 @@ __device__ __forceinline__ void warp_take_best(RowState& st, float cb, int ci) {
   }
 }
 
-// Exact scores of the entries in `cand` (bit e = entry v+e), merged into st.
-__device__ __forceinline__ void decide(RowState& st, uint32_t cand,
-                                       const float (&s)[4], const uint4 w,
-                                       bool greedy, int v) {
+// Philox4x32-10 block with precomputed round keys (same function as
+// philox4x32_10: the published multipliers; key + r * Weyl constants).
+__device__ __forceinline__ uint4 philox_rk(uint4 c, const uint32_t* rk) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long pa = (unsigned long long)0xD2511F53u * c.x;
+    const unsigned long long pb = (unsigned long long)0xCD9E8D57u * c.z;
+    c = make_uint4((uint32_t)(pb >> 32) ^ c.y ^ rk[2 * r], (uint32_t)pb,
+                   (uint32_t)(pa >> 32) ^ c.w ^ rk[2 * r + 1], (uint32_t)pa);
+  }
+  return c;
+}
+
+__device__ __forceinline__ uint4 row_noise(const RowConst& rc, int v) {
+  return philox_rk(make_uint4((uint32_t)v >> 2, rc.c1, rc.c2, rc.c3), rc.rk);
+}
+
+// Exact decision scores of the sampled entries in `cand`, merged into st.
+__device__ __forceinline__ void decide_sampled(RowState& st, uint32_t cand,
+                                               const float (&s)[4],
+                                               const uint4 w, int v) {
   float cb = -INFINITY;
   int ci = kNoIndex;
   while (cand) {
     const int e = __ffs(cand) - 1;
     cand &= cand - 1u;
-    const float se = pick4(s, e);
-    const float sc = greedy ? se : exact_score(se, word_of(w, e));
+    const float sc =
+        __fadd_rn(pick4(s, e), -logf(exponential_from_word(word_of(w, e))));
     if (sc > cb) {  // e ascending: strict keeps the lower index
       cb = sc;
       ci = v + e;
@@ -201,60 +215,11 @@ __device__ __forceinline__ void decide(RowState& st, uint32_t cand,
   warp_take_best(st, cb, ci);
 }
 
-// Four entries v..v+3 of one request (biased logits l from shared memory):
-// scaled logits, the decision, and the sum-exp.
-template <bool kUnitT>
-__device__ __forceinline__ void process4(const RowInfo& ri, const float4 l4,
-                                         bool valid, int v, RowState& st,
-                                         int k, float T) {
-  float s[4];
-  s[0] = valid ? scale<kUnitT>(l4.x, T) : -INFINITY;
-  s[1] = valid ? scale<kUnitT>(l4.y, T) : -INFINITY;
-  s[2] = valid ? scale<kUnitT>(l4.z, T) : -INFINITY;
-  s[3] = valid ? scale<kUnitT>(l4.w, T) : -INFINITY;
-  const uint4 w = noise_block(ri.seed, ri.offset, k, kNoiseDraft, (uint32_t)v >> 2);
-  const bool greedy = ri.greedy != 0;
-  float f[4];
-  const float old_best = st.best;
-  if (old_best == -INFINITY) {
-    // Nothing has won yet (the first tile of the chunk): decide each lane's
-    // largest entry exactly, then test the others against that best.
-    uint32_t first = 0;
-    float top = -INFINITY;
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (s[e] > top) {
-        top = s[e];
-        first = 1u << e;
-      }
-    if (__any_sync(0xffffffffu, first != 0u)) decide(st, first, s, w, greedy, v);
-    const float tc = thr_const(st.best);
-    uint32_t cand = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      f[e] = test_value(s[e], tc);
-      const bool c = greedy ? s[e] > st.best : __uint2float_rz(word_of(w, e)) < f[e];
-      cand |= (c ? 1u : 0u) << e;
-    }
-    cand &= ~first;
-    if (__any_sync(0xffffffffu, cand != 0u)) decide(st, cand, s, w, greedy, v);
-  } else {
-    const float tc = thr_const(old_best);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
-    uint32_t cand;
-    if (greedy) {
-      cand = (s[0] > old_best ? 1u : 0u) | (s[1] > old_best ? 2u : 0u) |
-             (s[2] > old_best ? 4u : 0u) | (s[3] > old_best ? 8u : 0u);
-    } else {
-      cand = (__uint2float_rz(w.x) < f[0] ? 1u : 0u) |
-             (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
-             (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
-             (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
-    }
-    if (__any_sync(0xffffffffu, cand != 0u)) decide(st, cand, s, w, greedy, v);
-  }
-  if (st.best != old_best) {  // a new reference for the sum (warp-uniform)
+// The sum-exp of four entries relative to the request's best (after the
+// decision): f = 2^(32+slack) exp(s - best) are the candidate-test values.
+__device__ __forceinline__ void add_sum(RowState& st, float old_best,
+                                        const float (&s)[4], float (&f)[4]) {
+  if (st.best != old_best) {  // new reference (the same in every lane)
     if (old_best != -INFINITY) st.sum *= ex2_approx((old_best - st.best) * kLog2e);
     const float tc = thr_const(st.best);
 #pragma unroll
@@ -267,6 +232,100 @@ __device__ __forceinline__ void process4(const RowInfo& ri, const float4 l4,
     st.sum = fmaf(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
                   kSumScale, st.sum);
   }
+}
+
+// Steady state of a sampled request (its best is finite): the conservative
+// test for every entry, exact scores for the few that pass.
+__device__ __forceinline__ void sampled_step(const RowConst& rc,
+                                             const float (&s)[4], int v,
+                                             RowState& st) {
+  const uint4 w = row_noise(rc, v);
+  const float old_best = st.best;
+  const float tc = thr_const(old_best);
+  float f[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+  const uint32_t cand = (__uint2float_rz(w.x) < f[0] ? 1u : 0u) |
+                        (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
+                        (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
+                        (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
+  if (__any_sync(0xffffffffu, cand != 0u)) decide_sampled(st, cand, s, w, v);
+  add_sum(st, old_best, s, f);
+}
+
+// Approximate decision score s - log E, used only to choose which entry of
+// a chunk's first tile to decide exactly (accuracy does not matter for the
+// result: every entry is then tested conservatively against the exact best).
+__device__ __forceinline__ float rough_score(float s, uint32_t x) {
+  const float w = fmaf(__uint2float_rz(x), 0x1p-32f, 0x1p-33f);
+  const float e = w < 0x1p-10f ? w : -__logf(__fsub_rn(1.0f, w));
+  return s - __logf(e);
+}
+
+// First tile of a sampled request (nothing has won yet): each lane decides
+// its roughly best entry exactly, the warp keeps the best of those, then
+// the remaining entries go through the conservative test.
+__device__ __forceinline__ void sampled_first(const RowConst& rc,
+                                              const float (&s)[4], int v,
+                                              RowState& st) {
+  const uint4 w = row_noise(rc, v);
+  uint32_t first = 0;
+  float top = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float a = s[e] == -INFINITY ? -INFINITY : rough_score(s[e], word_of(w, e));
+    if (a > top) {
+      top = a;
+      first = 1u << e;
+    }
+  }
+  decide_sampled(st, first, s, w, v);
+  const float tc = thr_const(st.best);
+  float f[4];
+  uint32_t cand = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    f[e] = test_value(s[e], tc);
+    cand |= (__uint2float_rz(word_of(w, e)) < f[e] ? 1u : 0u) << e;
+  }
+  cand &= ~first;
+  if (__any_sync(0xffffffffu, cand != 0u)) decide_sampled(st, cand, s, w, v);
+  add_sum(st, -INFINITY, s, f);
+}
+
+// A greedy request: no noise; an entry is a candidate iff s > best.
+__device__ __forceinline__ void greedy_step(const float (&s)[4], int v,
+                                            RowState& st) {
+  const float old_best = st.best;
+  uint32_t cand = (s[0] > old_best ? 1u : 0u) | (s[1] > old_best ? 2u : 0u) |
+                  (s[2] > old_best ? 4u : 0u) | (s[3] > old_best ? 8u : 0u);
+  if (__any_sync(0xffffffffu, cand != 0u)) {
+    float cb = -INFINITY;
+    int ci = kNoIndex;
+    while (cand) {
+      const int e = __ffs(cand) - 1;
+      cand &= cand - 1u;
+      if (pick4(s, e) > cb) {
+        cb = pick4(s, e);
+        ci = v + e;
+      }
+    }
+    warp_take_best(st, cb, ci);
+  }
+  float f[4];
+  const float tc = thr_const(st.best);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+  add_sum(st, st.best, s, f);
+}
+
+template <bool kUnitT>
+__device__ __forceinline__ void scaled4(const float4 l4, bool valid, float T,
+                                        float (&s)[4]) {
+  s[0] = valid ? scale<kUnitT>(l4.x, T) : -INFINITY;
+  s[1] = valid ? scale<kUnitT>(l4.y, T) : -INFINITY;
+  s[2] = valid ? scale<kUnitT>(l4.z, T) : -INFINITY;
+  s[3] = valid ? scale<kUnitT>(l4.w, T) : -INFINITY;
 }
 
 template <typename BT, bool kUnitT>
@@ -283,7 +342,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   uint8_t* u_s = smem + P.u_off;
   float* tiles = reinterpret_cast<float*>(smem + P.tile_off);
   const BT* stage = reinterpret_cast<const BT*>(smem + P.stage_off);
-  RowInfo* rows = reinterpret_cast<RowInfo*>(smem + P.rows_off);
+  RowConst* rows = reinterpret_cast<RowConst*>(smem + P.rows_off);
   const int S = P.stages;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + P.bar_off);
   uint64_t* empty = full + S;
@@ -358,17 +417,26 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
                                 ((p ^ (b & 7)) << 4)) = val;
     }
     for (int b = ct; b < P.bpad; b += kComputeThreads) {
-      RowInfo ri;
+      RowConst rc;
+      uint32_t k0 = 0, k1 = 0;
+      rc.c1 = (uint32_t)P.k | ((uint32_t)kNoiseDraft << 16);
+      rc.c2 = rc.c3 = 0;
+      rc.flags = 0;
       if (b < a.B) {
-        ri.seed = a.seed[b];
-        ri.offset = a.offset[b];
-        ri.pad = a.pad_row != nullptr && a.pad_row[b] != 0;
-        ri.greedy = a.greedy != nullptr && a.greedy[b] != 0;
-      } else {
-        ri.seed = ri.offset = 0;
-        ri.pad = ri.greedy = 0;
+        k0 = (uint32_t)a.seed[b];
+        k1 = (uint32_t)(a.seed[b] >> 32);
+        rc.c2 = (uint32_t)a.offset[b];
+        rc.c3 = (uint32_t)(a.offset[b] >> 32);
+        rc.flags = (a.pad_row != nullptr && a.pad_row[b] != 0 ? kRowPad : 0u) |
+                   (a.greedy != nullptr && a.greedy[b] != 0 ? kRowGreedy : 0u);
       }
-      rows[b] = ri;
+      for (int r = 0; r < 10; ++r) {
+        rc.rk[2 * r] = k0;
+        rc.rk[2 * r + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+      }
+      rows[b] = rc;
     }
     fence_proxy_async_smem();
   }
@@ -494,7 +562,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     // drained columns that hold requests (< B), and which are padding rows
     const int nvalid = a.B - col0 < 0 ? 0 : (a.B - col0 < gcols ? a.B - col0 : gcols);
     uint32_t padmask = 0;
-    for (int c = 0; c < nvalid; ++c) padmask |= (rows[col0 + c].pad ? 1u : 0u) << c;
+    for (int c = 0; c < nvalid; ++c)
+      padmask |= ((rows[col0 + c].flags & kRowPad) ? 1u : 0u) << c;
     const float T = a.T;
     const int V = a.V;
     RowState st[kMaxRows];
@@ -565,7 +634,15 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           const int b = cw + kComputeWarps * i;
           if (b >= a.B) break;
           const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
-          process4<kUnitT>(rows[b], l4, valid, v, st[i], P.k, T);
+          float sv[4];
+          scaled4<kUnitT>(l4, valid, T, sv);
+          const RowConst& rc = rows[b];
+          if (rc.flags & kRowGreedy)
+            greedy_step(sv, v, st[i]);
+          else if (st[i].best == -INFINITY)
+            sampled_first(rc, sv, v, st[i]);
+          else
+            sampled_step(rc, sv, v, st[i]);
         }
       }
       if (storer) bulk_wait_read_all();  // the store has read the tile
@@ -632,7 +709,7 @@ Layout make_layout(int B, int r, int base_elt) {
   const size_t u = (size_t)L.bpad * r * 2;
   const size_t tiles = 2 * (size_t)L.bpad * kTileV * 4;
   const size_t stage = base_elt == 2 ? (size_t)L.bpad * kTileV * 2 : 0;
-  const size_t rows = align_up((size_t)L.bpad * sizeof(RowInfo), 16);
+  const size_t rows = align_up((size_t)L.bpad * sizeof(RowConst), 16);
   const size_t bars = (2 * kMaxStages + 10) * 8 + 16;
   const size_t fixed = u + tiles + stage + rows + bars + 1024;
   L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
