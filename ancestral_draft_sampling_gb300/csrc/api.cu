@@ -321,7 +321,7 @@ dspark_status dspark_verify_standard(const float* draft_probs,
     return DSPARK_ERR_UNSUPPORTED;
   return from_cuda(launch_verify(draft_probs, target_probs, tokens, seed,
                                  offset, B, K, V, accepted_len, emitted_token,
-                                 stream));
+                                 sm_count(), stream));
 }
 
 dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,

@@ -239,7 +239,7 @@ cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream);
 cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           const uint64_t* seed, const uint64_t* offset, int B,
                           int K, int V, int32_t* accepted_len,
-                          int32_t* emitted, cudaStream_t stream);
+                          int32_t* emitted, int sms, cudaStream_t stream);
 cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
                                int stream_id, int n, uint32_t* out,
                                float* gumbel, cudaStream_t stream);

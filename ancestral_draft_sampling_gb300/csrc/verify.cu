@@ -7,110 +7,290 @@
 // drawn from the residual norm(max(p_k - q_k, 0)); if all K drafts pass, a
 // bonus token is drawn from p_K.
 //
-// One CTA per request.  Thread 0 walks the K acceptance tests (one uniform
-// each, noise stream 1); then the whole CTA does one Gumbel-max sweep over
-// the drawing row (noise stream 2 at the drawing position).
+// One thread-block cluster of C CTAs per request (C chosen so the grid fills
+// the GPU).  Every CTA of the cluster runs the K acceptance tests itself (one
+// thread per draft, one uniform each from noise stream 1; the first rejection
+// is a shared-memory minimum), then draws from its own slice of the drawing
+// row by Gumbel-max over log(weight) with noise stream 2 at the drawing
+// position; the C partial winners merge through distributed shared memory.
+//
+// In a slice, warps sweep 128 entries per step, lane l on one Philox block of
+// 4 entries.  An entry with weight r and exponential variate E can only beat
+// the warp's best score B if log r - log E > B, i.e. E < r e^-B, which needs
+// w < r e^-B since E = -log(1 - w) >= w; so the test
+// (float)x < 2^32 r e^-B (1 + 2^-11) admits every possible winner (the slack
+// covers the float32 rounding of both scores) with a multiply and a compare,
+// and only entries that pass get the exact score.  Candidates merge by a
+// max-reduction over order-preserving score bits, then a min over indices.
+#include <cooperative_groups.h>
+
 #include "dspark_common.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr int kVerifyThreads = 512;
+namespace cg = cooperative_groups;
 
-struct Cand {
+constexpr int kVerifyThreads = 256;
+constexpr int kVerifyWarps = kVerifyThreads / 32;
+constexpr int kVerifyMinBlocks = 4;   // resident CTAs per SM the launch asks for
+constexpr int kMaxCluster = 8;        // portable cluster size
+constexpr int kMinSliceBlocks = 1024; // Philox blocks (4 entries) per CTA, at least
+constexpr float kSlack = 1.000489f;   // 1 + 2^-11, rounded up
+// Above this best score e^-B leaves the normal range of float32; the test
+// then admits everything (still exact, only slower).  Scores that large need
+// weights above e^57.
+constexpr float kMaxTestScore = 80.0f;
+
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered_bits(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+struct Best {
   float score;
   int idx;
 };
 
-// Keeps the better of c and (score, idx): larger score, then lower index.
-__device__ __forceinline__ void take(Cand& c, float score, int idx) {
-  if (better(c.score, c.idx, score, idx)) return;
-  c.score = score;
-  c.idx = idx;
-}
+struct alignas(16) Slot {
+  float score;
+  int idx;
+  int any;
+  int pad;
+};
 
-__device__ __forceinline__ Cand block_argmax(Cand c, Cand* part) {
-#pragma unroll
-  for (int mask = 16; mask > 0; mask >>= 1) {
-    const float os = __shfl_xor_sync(0xffffffffu, c.score, mask);
-    const int oi = __shfl_xor_sync(0xffffffffu, c.idx, mask);
-    take(c, os, oi);
+// Keeps the better of st and the warp's candidates (larger score, then the
+// lower index); lanes without a candidate offer key 0.
+__device__ __forceinline__ void warp_take(Best& st, float cb, int ci) {
+  const uint32_t key = ci == kNoIndex ? 0u : ordered_bits(cb);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  if (kmax == 0u) return;
+  const uint32_t imin =
+      __reduce_min_sync(0xffffffffu, key == kmax ? (uint32_t)ci : 0xffffffffu);
+  const float wb = from_ordered_bits(kmax);
+  if (better(wb, (int)imin, st.score, st.idx)) {
+    st.score = wb;
+    st.idx = (int)imin;
   }
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) part[warp] = c;
-  __syncthreads();
-  c = part[0];
-  for (int w = 1; w < kVerifyThreads / 32; ++w) take(c, part[w].score, part[w].idx);
-  return c;
 }
 
-__global__ void __launch_bounds__(kVerifyThreads)
+__device__ __forceinline__ float elem(const float4 v, int e) {
+  return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// Loads Philox block j (entries 4j .. 4j+3) of p and, for the residual, q;
+// entries at or beyond V read as 0.
+template <bool kVec>
+__device__ __forceinline__ void load_block(const float* __restrict__ p,
+                                           const float* __restrict__ q, int V,
+                                           int j, int hi, float4& pv,
+                                           float4& qv) {
+  pv = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  qv = pv;
+  if (j >= hi) return;
+  if (kVec) {
+    pv = __ldcs(reinterpret_cast<const float4*>(p) + j);
+    if (q) qv = __ldcs(reinterpret_cast<const float4*>(q) + j);
+  } else {
+    float* pp = &pv.x;
+    float* qq = &qv.x;
+    for (int e = 0; e < 4; ++e)
+      if (4 * j + e < V) {
+        pp[e] = __ldcs(p + 4 * j + e);
+        if (q) qq[e] = __ldcs(q + 4 * j + e);
+      }
+  }
+}
+
+// One Philox block of the sweep: weights, candidate test, exact scores of
+// the candidates, warp merge.  Warp-uniform control flow.
+__device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
+                                            float4 pv, float4 qv, bool resid,
+                                            uint64_t seed, uint64_t offset,
+                                            int pos) {
+  float wt[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float pe = elem(pv, e);
+    const float d = resid ? __fsub_rn(pe, elem(qv, e)) : pe;
+    wt[e] = d > 0.0f ? d : 0.0f;  // NaN and non-positive weights: 0
+    any |= wt[e] > 0.0f;
+  }
+  const uint4 w = noise_block(seed, offset, pos, kNoiseResample, (uint32_t)j);
+  // 2^32 (1 + slack) e^-best; +inf (everything is a candidate) while nothing
+  // has won or e^-best is out of float32's normal range
+  const float c = (st.idx == kNoIndex || st.score > kMaxTestScore)
+                      ? INFINITY
+                      : 0x1p32f * kSlack * expf(-st.score);
+  uint32_t cand = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float thr = wt[e] > 0.0f ? __fmul_ru(wt[e], c) : 0.0f;
+    cand |= (__uint2float_rz(word_of(w, e)) < thr ? 1u : 0u) << e;
+  }
+  if (__any_sync(0xffffffffu, cand != 0u)) {
+    float cb = -INFINITY;
+    int ci = kNoIndex;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (!((cand >> e) & 1u)) continue;
+      const float sc = __fadd_rn(logf(wt[e]), gumbel_from_word(word_of(w, e)));
+      if (ci == kNoIndex || sc > cb) {  // e ascending: keeps the lower index
+        cb = sc;
+        ci = 4 * j + e;
+      }
+    }
+    warp_take(st, cb, ci);
+  }
+}
+
+// Gumbel-max over log(weight) on this CTA's slice [lo, hi) of Philox blocks,
+// weights max(p - q, 0) when q != nullptr (the residual), else p; zero
+// weights never win.  Then the cluster-wide winner and "some weight was
+// positive", identical in every CTA of the cluster.
+template <bool kVec>
+__device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p,
+                         const float* __restrict__ q, int V, int lo, int hi,
+                         uint64_t seed, uint64_t offset, int pos, Best* part,
+                         int* any_part, Slot* slot) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool resid = q != nullptr;
+  Best st = {-INFINITY, kNoIndex};
+  bool any = false;
+  constexpr int kStride = kVerifyWarps * 32;
+  // two blocks per lane in flight: j and j + kStride
+  for (int base = lo + warp * 32; base < hi; base += 2 * kStride) {
+    const int j0 = base + lane, j1 = base + kStride + lane;
+    float4 p0, q0, p1, q1;
+    load_block<kVec>(p, q, V, j0, hi, p0, q0);
+    load_block<kVec>(p, q, V, j1, hi, p1, q1);
+    sweep_block(st, any, j0, p0, q0, resid, seed, offset, pos);
+    if (base + kStride < hi)
+      sweep_block(st, any, j1, p1, q1, resid, seed, offset, pos);
+  }
+  any = __any_sync(0xffffffffu, any);
+  if (lane == 0) {
+    part[warp] = st;
+    any_part[warp] = any;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Best r = part[0];
+    int a = any_part[0];
+    for (int i = 1; i < kVerifyWarps; ++i) {
+      if (!better(r.score, r.idx, part[i].score, part[i].idx)) r = part[i];
+      a |= any_part[i];
+    }
+    *slot = Slot{r.score, r.idx, a, 0};
+  }
+  cluster.sync();  // every CTA's slot is written
+  Slot all = *cluster.map_shared_rank(slot, 0u);
+  for (unsigned i = 1; i < cluster.num_blocks(); ++i) {
+    const Slot o = *cluster.map_shared_rank(slot, i);
+    if (!better(all.score, all.idx, o.score, o.idx)) {
+      all.score = o.score;
+      all.idx = o.idx;
+    }
+    all.any |= o.any;
+  }
+  cluster.sync();  // every CTA has read every slot (they may be rewritten)
+  return all;
+}
+
+template <bool kVec>
+__global__ void __launch_bounds__(kVerifyThreads, kVerifyMinBlocks)
 verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
               const int32_t* __restrict__ tokens, const uint64_t* seed,
               const uint64_t* offset, int K, int V, int32_t* accepted_len,
               int32_t* emitted) {
-  __shared__ int s_draw_pos;
+  __shared__ int s_first;
   __shared__ int s_bad;
-  __shared__ Cand part[kVerifyThreads / 32];
-  const int b = blockIdx.x;
+  __shared__ Best part[kVerifyWarps];
+  __shared__ int any_part[kVerifyWarps];
+  __shared__ Slot slot;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int C = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  const int b = blockIdx.x / C;
   const uint64_t sd = seed[b], off = offset[b];
   if (threadIdx.x == 0) {
-    int kk = K, bad = 0;
-    for (int k = 0; k < K; ++k) {
-      const int d = tokens[(size_t)b * K + k];
-      if (d < 0 || d >= V) {
-        bad = 1;
-        break;
-      }
-      const float qd = q[((size_t)b * K + k) * V + d];
-      const float pd = p[((size_t)b * (K + 1) + k) * V + d];
-      const float u = accept_uniform(noise_block(sd, off, k, kNoiseAccept, 0u).x);
-      if (!(__fmul_rn(u, qd) < pd)) {
-        kk = k;
-        break;
-      }
-    }
-    s_draw_pos = kk;
-    s_bad = bad;
+    s_first = K;
+    s_bad = 0;
   }
   __syncthreads();
-  if (s_bad) {
-    if (threadIdx.x == 0) {
+  for (int k = threadIdx.x; k < K; k += kVerifyThreads) {
+    const int d = tokens[(size_t)b * K + k];
+    if (d < 0 || d >= V) {
+      atomicOr(&s_bad, 1);
+      continue;
+    }
+    const float qd = q[((size_t)b * K + k) * V + d];
+    const float pd = p[((size_t)b * (K + 1) + k) * V + d];
+    const float u = accept_uniform(noise_block(sd, off, k, kNoiseAccept, 0u).x);
+    if (!(__fmul_rn(u, qd) < pd)) atomicMin(&s_first, k);
+  }
+  __syncthreads();
+  if (s_bad) {  // the same in every CTA of the cluster: all return here
+    if (rank == 0 && threadIdx.x == 0) {
       accepted_len[b] = -1;
       emitted[b] = -1;
     }
     return;
   }
-  const int kk = s_draw_pos;
+  const int kk = s_first;
   const float* prow = p + ((size_t)b * (K + 1) + kk) * V;
   const float* qrow = kk < K ? q + ((size_t)b * K + kk) * V : nullptr;
-  Cand res = {-INFINITY, kNoIndex};  // residual draw
-  Cand tgt = {-INFINITY, kNoIndex};  // draw from p itself
+  // this CTA's slice of the row's Philox blocks
   const int n_blk = (V + 3) / 4;
-  for (int j = threadIdx.x; j < n_blk; j += kVerifyThreads) {
-    const uint4 w = noise_block(sd, off, kk, kNoiseResample, (uint32_t)j);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int v = 4 * j + e;
-      if (v >= V) break;
-      const float g = gumbel_from_word(word_of(w, e));
-      const float pv = prow[v];
-      if (pv > 0.0f) take(tgt, __fadd_rn(logf(pv), g), v);
-      if (qrow) {
-        const float diff = __fsub_rn(pv, qrow[v]);
-        if (diff > 0.0f) take(res, __fadd_rn(logf(diff), g), v);
-      }
-    }
-  }
-  res = block_argmax(res, part);
-  tgt = block_argmax(tgt, part);
-  if (threadIdx.x == 0) {
-    int tok = (qrow && res.idx != kNoIndex) ? res.idx : tgt.idx;
-    if (tok == kNoIndex) tok = 0;
+  const int per = (n_blk + C - 1) / C;
+  const int lo = min(rank * per, n_blk), hi = min(lo + per, n_blk);
+  Slot r = draw_row<kVec>(cluster, prow, qrow, V, lo, hi, sd, off, kk, part,
+                          any_part, &slot);
+  if (qrow != nullptr && !r.any)  // residual all zero: draw from p itself
+    r = draw_row<kVec>(cluster, prow, nullptr, V, lo, hi, sd, off, kk, part,
+                       any_part, &slot);
+  if (rank == 0 && threadIdx.x == 0) {
     accepted_len[b] = kk;
-    emitted[b] = tok;
+    emitted[b] = r.idx == kNoIndex ? 0 : r.idx;
   }
+}
+
+// CTAs per request: enough clusters to fill every SM's resident slots, at
+// most the portable cluster size, and at least kMinSliceBlocks per slice.
+int verify_cluster_size(int B, int V, int sms) {
+  const int slots = sms * kVerifyMinBlocks;
+  int c = slots / (B > 0 ? B : 1);
+  const int n_blk = (V + 3) / 4;
+  const int by_len = n_blk / kMinSliceBlocks;
+  if (c > by_len) c = by_len;
+  if (c > kMaxCluster) c = kMaxCluster;
+  return c < 1 ? 1 : c;
+}
+
+template <bool kVec>
+cudaError_t launch_verify_t(const float* q, const float* p,
+                            const int32_t* tokens, const uint64_t* seed,
+                            const uint64_t* offset, int B, int K, int V,
+                            int32_t* accepted_len, int32_t* emitted, int C,
+                            cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B * (unsigned)C, 1, 1);
+  cfg.blockDim = dim3(kVerifyThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, verify_kernel<kVec>, q, p, tokens, seed,
+                            offset, K, V, accepted_len, emitted);
 }
 
 }  // namespace
@@ -118,10 +298,13 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
 cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           const uint64_t* seed, const uint64_t* offset, int B,
                           int K, int V, int32_t* accepted_len,
-                          int32_t* emitted, cudaStream_t stream) {
-  verify_kernel<<<B, kVerifyThreads, 0, stream>>>(q, p, tokens, seed, offset,
-                                                  K, V, accepted_len, emitted);
-  return cudaGetLastError();
+                          int32_t* emitted, int sms, cudaStream_t stream) {
+  const int C = verify_cluster_size(B, V, sms);
+  if (V % 4 == 0)
+    return launch_verify_t<true>(q, p, tokens, seed, offset, B, K, V,
+                                 accepted_len, emitted, C, stream);
+  return launch_verify_t<false>(q, p, tokens, seed, offset, B, K, V,
+                                accepted_len, emitted, C, stream);
 }
 
 }  // namespace dspark

@@ -136,6 +136,61 @@ def make_custom(B, K, V, r, *, seed=1, base_std=3.0, w_std=0.02,
                     offset=offs, greedy=greedy, pad_row=pad, target=tgt)
 
 
+@dataclasses.dataclass
+class VerifyInputs:
+    """Inputs of standard verification for B requests of K drafts."""
+    B: int
+    K: int
+    V: int
+    q: np.ndarray        # [B,K,V] float32: the proposals the drafts came from
+    p: np.ndarray        # [B,K+1,V] float32: the target's distributions
+    tokens: np.ndarray   # [B,K] int32: drafts, token k drawn from q[b,k]
+    seed: np.ndarray     # [B] uint64
+    offset: np.ndarray   # [B] uint64
+
+
+def _softmax_rows(x: np.ndarray) -> np.ndarray:
+    x = x.astype(np.float64)
+    x -= x.max(axis=-1, keepdims=True)
+    np.exp(x, out=x)
+    x /= x.sum(axis=-1, keepdims=True)
+    return x
+
+
+def make_verify(B, K, V, *, seed=1, logit_std=3.0, target_noise=1.0,
+                n_spikes=32, spike=12.0, req_seed0=1234,
+                offset=0) -> VerifyInputs:
+    """Synthetic verification inputs: per request, drafter logits
+    ~N(0, logit_std^2) plus n_spikes spikes per row; q = softmax of them;
+    target row k < K = softmax(logits_k + N(0, target_noise^2)), the bonus
+    row K = softmax(logits_{K-1} + fresh noise); draft k is drawn from q_k
+    by numpy's generator (inverse CDF), so acceptance rates are those of a
+    drafter that is this close to the target."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = np.empty((B, K, V), dtype=np.float32)
+    p = np.empty((B, K + 1, V), dtype=np.float32)
+    tokens = np.empty((B, K), dtype=np.int32)
+    for b in range(B):  # one request at a time keeps the float64 rows small
+        logits = _normal(rng, (1, K, V), logit_std)
+        if n_spikes:
+            _spike(rng, logits, min(n_spikes, V), spike)
+        logits = logits[0]
+        qb = _softmax_rows(logits)
+        q[b] = qb
+        tgt = np.concatenate([logits, logits[K - 1:K]], axis=0)
+        tgt = tgt + _normal(rng, (K + 1, V), target_noise)
+        p[b] = _softmax_rows(tgt)
+        cdf = np.cumsum(qb, axis=1)
+        u = rng.random(K) * cdf[:, -1]
+        for k in range(K):
+            tokens[b, k] = min(int(np.searchsorted(cdf[k], u[k], side="right")),
+                               V - 1)
+    seeds = np.arange(B, dtype=np.uint64) + np.uint64(req_seed0)
+    offs = np.full(B, offset, dtype=np.uint64)
+    return VerifyInputs(B=B, K=K, V=V, q=q, p=p, tokens=tokens, seed=seeds,
+                        offset=offs)
+
+
 CONFIG_NAMES = {1: "small", 2: "b8", 3: "b44", 4: "b88", 5: "b64v"}
 
 

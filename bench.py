@@ -162,6 +162,21 @@ def ncu_traffic(kernel: str):
         return None
 
 
+def job_timing(ms_total_local, steps, world, dist=None, device="cpu"):
+    """Whole-job timing of N independent replicas: the slowest rank's time
+    (max over ranks) per step, and whole-job µs per block = that time / N
+    (the N replicas each draft one block per step)."""
+    ms_total = float(ms_total_local)
+    if dist is not None and world > 1:
+        import torch
+        t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+    ms_step = ms_total / steps
+    return ms_step, ms_step * 1e3 / world
+
+
 # ------------------------------------------------------------ CPU oracle
 def oracle_block_seconds(w, n_requests: int, threads: int):
     """Wall seconds for the oracle to draft `n_requests` requests (all K
@@ -306,14 +321,8 @@ def run_ours(args, rank, world):
             graph.replay()
         ev1.record(cur)
         torch.cuda.synchronize()
-    ms_total = ev0.elapsed_time(ev1)
-    if dist:
-        t = torch.tensor([ms_total], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
-        dist.barrier()
-    ms_step = ms_total / args.steps
-    us_per_block = ms_step * 1e3 / world  # whole job: N replicas in parallel
+    ms_step, us_per_block = job_timing(ev0.elapsed_time(ev1), args.steps,
+                                       world, dist, "cuda")
 
     # per-kernel durations, CUDA events around every launch on its stream
     prof = {"position": [0.0, 0], "pick": [0.0, 0], "proposal": [0.0, 0]}
@@ -377,6 +386,36 @@ def run_ours(args, rank, world):
         t.numel() * t.element_size() for t in host_small.values())
     d2h = host_tokens.numel() * 4
 
+    # secondary path: standard verification of this block's drafts against
+    # target distributions softmax(l + N(0,1)) (timing inputs, made by torch)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    tl = torch.cat([logits, logits[:, -1:]], dim=1)
+    tl = tl + torch.randn(tl.shape, device="cuda", generator=gen)
+    target = torch.softmax(tl.nan_to_num(neginf=-1e30), dim=-1)
+    del tl
+    acc_len = torch.empty(B, dtype=torch.int32, device="cuda")
+    emitted = torch.empty(B, dtype=torch.int32, device="cuda")
+    for _ in range(3):
+        pkg.verify_standard(probs, target, tokens, dev["seed"], dev["offset"],
+                            accepted_len=acc_len, emitted_token=emitted)
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_ver = 20
+    f0.record(cur)
+    for _ in range(n_ver):
+        pkg.verify_standard(probs, target, tokens, dev["seed"], dev["offset"],
+                            accepted_len=acc_len, emitted_token=emitted)
+    f1.record(cur)
+    torch.cuda.synchronize()
+    verify_us = f0.elapsed_time(f1) / n_ver * 1e3
+    verify = {"us_per_call": verify_us, "B": B, "K": K, "V": V,
+              "mean_accepted_len": float(acc_len.float().mean().item()),
+              "upper_bound_bytes": B * V * 8,
+              "note": "standard rejection verification of the benchmark "
+                      "block's drafts (one thread-block cluster of CTAs per request)"}
+    del target
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": us_per_block, "unit": "us",
@@ -391,6 +430,7 @@ def run_ours(args, rank, world):
             "compulsory_bytes_per_block": compulsory_bytes(w),
             "roofline": roofline,
             "clocks": clocks.summary(),
+            "verify": verify,
             "gpu_launches": args.steps * (2 * K + 1),
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,

@@ -70,7 +70,7 @@ def _load():
             P, P, P, P, P, P, P, P]
         lib.oracle_draft_position.restype = I
         lib.oracle_draft_block.argtypes = [
-            P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P,
+            P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I,
             P, P, P, P, P, P]
         lib.oracle_draft_block.restype = I
         lib.oracle_verify_standard.argtypes = [P, P, P, P, P, I, I, I, P, P,
@@ -159,8 +159,8 @@ class BlockResult:
     __slots__ = ("tokens", "logits", "probs", "rowstats", "top2")
 
 
-def draft_block(base, U, Wb, d0, seed, offset, T, greedy=None, pad_row=None,
-                force_tokens=None) -> BlockResult:
+def draft_block(base, U, Wb, d0, seed, offset, T, greedy=None,
+                pad_row=None) -> BlockResult:
     """The whole ancestral block, row after row (single thread)."""
     lib = _load()
     B, K, V = base.shape
@@ -173,8 +173,6 @@ def draft_block(base, U, Wb, d0, seed, offset, T, greedy=None, pad_row=None,
     offset = np.ascontiguousarray(offset, dtype=np.uint64)
     g = None if greedy is None else np.ascontiguousarray(greedy, dtype=np.uint8)
     p = None if pad_row is None else np.ascontiguousarray(pad_row, dtype=np.uint8)
-    f = (None if force_tokens is None
-         else np.ascontiguousarray(force_tokens, dtype=np.int32))
     out = BlockResult()
     out.tokens = np.zeros((B, K), dtype=np.int32)
     out.logits = np.empty((B, K, V), dtype=np.float32)
@@ -185,32 +183,40 @@ def draft_block(base, U, Wb, d0, seed, offset, T, greedy=None, pad_row=None,
     rc = lib.oracle_draft_block(
         _ptr(base), _dtype_code(base), _ptr(U), _ptr(Wb), _dtype_code(U),
         _ptr(d0), _ptr(seed), _ptr(offset), float(T), _ptr(g), _ptr(p), B, K,
-        V, r, _ptr(f), _ptr(out.tokens), _ptr(out.logits), _ptr(out.probs),
+        V, r, _ptr(out.tokens), _ptr(out.logits), _ptr(out.probs),
         _ptr(out.rowstats), _ptr(out.top2), _ptr(scratch))
     if rc != 0:
         raise ValueError("oracle_draft_block rejected its arguments")
     return out
 
 
-def draft_rows(base, U, Wb, prev, seed, offset, T, rows, greedy=None,
-               pad_row=None, threads: int | None = None):
-    """Teacher-forced sample: for each (b, k) in ``rows`` compute that
-    position given ``prev[b, k]`` (the token that conditions it).  Rows are
-    independent, so they run on a thread pool (ctypes releases the GIL).
-    Returns a list of PositionResult in the order of ``rows``."""
-    threads = threads or max(1, min(len(rows), os.cpu_count() or 1))
+def draft_chains(base, U, Wb, d0, seed, offset, T, depth, greedy=None,
+                 pad_row=None, threads: int | None = None):
+    """Free-running chains: for each request b with depth[b] > 0, positions
+    0 .. depth[b]-1 in order, each conditioned on the oracle's own draw
+    before it (d0[b] for position 0), exactly as ``draft_block`` computes
+    them.  Requests are independent, so they run on a thread pool (ctypes
+    releases the GIL).  Returns {b: [PositionResult per position]}."""
+    todo = [b for b in range(len(depth)) if depth[b] > 0]
+    threads = threads or max(1, min(len(todo), os.cpu_count() or 1))
 
-    def one(bk):
-        b, k = bk
+    def one(b):
         is_pad = bool(pad_row[b]) if pad_row is not None else False
         is_greedy = bool(greedy[b]) if greedy is not None else False
-        row = None if is_pad else base[b, k]
-        return draft_position(row, U, Wb, int(prev[b, k]), int(seed[b]),
-                              int(offset[b]), k, T, greedy=is_greedy,
-                              is_pad=is_pad)
+        prev, chain = int(d0[b]), []
+        for k in range(int(depth[b])):
+            row = None if is_pad else base[b, k]
+            res = draft_position(row, U, Wb, prev, int(seed[b]),
+                                 int(offset[b]), k, T, greedy=is_greedy,
+                                 is_pad=is_pad)
+            chain.append(res)
+            prev = res.token
+        return chain
 
+    if not todo:
+        return {}
     with ThreadPoolExecutor(max_workers=threads) as ex:
-        return list(ex.map(one, rows))
+        return dict(zip(todo, ex.map(one, todo)))
 
 
 class VerifyResult:

@@ -231,19 +231,14 @@ int oracle_draft_position(const void* base_row, int base_dtype, int is_pad,
  * order, each conditioned on the token drawn before it (d0[b] for k = 0).
  *
  * base [B,K,V] (base_dtype), U [V,r], Wb [r,V] (w_dtype), d0/seed/offset [B],
- * greedy/pad_row [B] or NULL.  force_tokens [B,K] or NULL: when given, the
- * token that conditions position k+1 is force_tokens[b,k] instead of the
- * oracle's own draw (used to follow another implementation's chain after an
- * allowed near-tie disagreement); tokens[] still receives the oracle's draws.
- * Outputs: tokens [B,K], logits [B,K,V] float32, probs [B,K,V] double,
+ * greedy/pad_row [B] or NULL.  Outputs: tokens [B,K], logits [B,K,V] float32, probs [B,K,V] double,
  * rowstats [B,K,2] (M, S) double, top2 [B,K,2] float (best, second) or NULL.
  */
 int oracle_draft_block(const void* base, int base_dtype, const void* U,
                        const void* Wb, int w_dtype, const int32_t* d0,
                        const uint64_t* seed, const uint64_t* offset, float T,
                        const uint8_t* greedy, const uint8_t* pad_row, int B,
-                       int K, int V, int r, const int32_t* force_tokens,
-                       int32_t* tokens, float* logits, double* probs,
+                       int K, int V, int r, int32_t* tokens, float* logits, double* probs,
                        double* rowstats, float* top2, double* bias_scratch) {
   if (B <= 0 || K <= 0) return -1;
   size_t elt = (base_dtype == ORACLE_F32) ? 4 : 2;
@@ -273,8 +268,7 @@ int oracle_draft_block(const void* base, int base_dtype, const void* U,
         top2[2 * row] = best;
         top2[2 * row + 1] = second;
       }
-      prev = force_tokens ? force_tokens[row] : token;
-      if (prev < 0 || prev >= V) return -1;
+      prev = token;
     }
   }
   return 0;

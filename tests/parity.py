@@ -12,9 +12,11 @@ Tolerances (the spec bar, with one derived widening):
                once, so l may differ by one ulp; exp(s - M) then moves by
                ulp(l) / T relative, which for T >= 0.7 and |l| < 32 stays
                below 1e-5 and for small T (e.g. 0.05) needs the 4-ulp term.
-Comparisons are teacher-forced: position k of request b is recomputed by the
-oracle from the token the GPU drew at k-1, so one allowed near-tie
-divergence does not shift the rest of the row.
+Comparisons are free-running: the oracle draws its own chain of every
+request from d0 and never sees a GPU output.  Where the GPU's token at (b, k)
+differs from the oracle's (allowed only at a near tie), the positions after
+k of request b have other inputs on the two sides and are not compared;
+such requests are counted.
 """
 from __future__ import annotations
 
@@ -79,24 +81,36 @@ def default_rows(B, K, max_rows=None, seed=0):
 def check_block_against_oracle(w, tokens, logits, probs, rows=None,
                                threads=None):
     """Asserts parity of the GPU outputs (numpy) on `rows` (default: all).
-    Returns a dict of counters (rows checked, near-tie token differences)."""
+    Returns a dict of counters (rows compared, near-tie token differences,
+    rows skipped after such a difference)."""
     B, K, V = w.B, w.K, w.V
     rows = rows or default_rows(B, K)
     assert tokens.shape == (B, K)
     assert ((tokens >= 0) & (tokens < V)).all(), "token out of range"
-    prev = np.concatenate([w.d0[:, None].astype(np.int32), tokens[:, :-1]], axis=1)
-    res = oracle.draft_rows(w.base, w.U, w.Wb, prev, w.seed, w.offset, w.T,
-                            rows, greedy=w.greedy, pad_row=w.pad_row,
-                            threads=threads)
-    ties = 0
-    for (b, k), o in zip(rows, res):
+    depth = np.zeros(B, dtype=np.int64)
+    for b, k in rows:
+        depth[b] = max(depth[b], k + 1)
+    chains = oracle.draft_chains(w.base, w.U, w.Wb, w.d0, w.seed, w.offset,
+                                 w.T, depth, greedy=w.greedy,
+                                 pad_row=w.pad_row, threads=threads)
+    # first position whose token differs from the oracle's draw, per request
+    diverged = {}
+    for b, chain in chains.items():
+        for k, o in enumerate(chain):
+            if tokens[b, k] != o.token:
+                gap = o.best - o.second
+                assert gap <= TOKEN_TIE, (
+                    f"token (b={b}, k={k}): gpu {tokens[b, k]} oracle "
+                    f"{o.token}, oracle top-2 gap {gap}")
+                diverged[b] = k
+                break
+    checked = skipped = 0
+    for b, k in rows:
+        if b in diverged and k > diverged[b]:
+            skipped += 1  # conditioned on different tokens: not comparable
+            continue
+        o = chains[b][k]
         where = f"(b={b}, k={k})"
-        if tokens[b, k] != o.token:
-            gap = o.best - o.second
-            assert gap <= TOKEN_TIE, (
-                f"token {where}: gpu {tokens[b, k]} oracle {o.token}, "
-                f"oracle top-2 gap {gap}")
-            ties += 1
         np.testing.assert_allclose(logits[b, k], o.logits, rtol=LOGIT_RTOL,
                                    atol=LOGIT_ATOL, equal_nan=True,
                                    err_msg=f"logits {where}")
@@ -111,7 +125,9 @@ def check_block_against_oracle(w, tokens, logits, probs, rows=None,
                 probs[b, k], o.probs, atol=PROB_ATOL,
                 rtol=prob_rtol(o.logits, w.T), equal_nan=True,
                 err_msg=f"draft_probs {where}")
-    return {"rows": len(rows), "near_tie_token_diffs": ties}
+        checked += 1
+    return {"rows": checked, "near_tie_token_diffs": len(diverged),
+            "rows_after_divergence": skipped}
 
 
 def run_draft(w, dev=None, device="cuda:0", stream=None, workspace=None):
