@@ -101,6 +101,7 @@ dspark_status prepare_draft(
   char* ws = static_cast<char*>(workspace);
   a.stats = reinterpret_cast<ChunkStat*>(ws + L.stats);
   a.rowstats = reinterpret_cast<float*>(ws + L.rowstats);
+  a.hints = reinterpret_cast<uint32_t*>(ws + L.hints);
   a.control = reinterpret_cast<int*>(ws + L.control);
 
   return DSPARK_OK;
@@ -158,6 +159,11 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   // merges them in slot order
   const int want = tc ? position_tc_chunks(a.V, sms) : sms;
   const int n_chunks = tc ? want : generic_chunks_used(a.V, want);
+  // the cross-CTA best-score hints of every position start empty
+  if (tc && cudaMemset2DAsync(a.hints, kHintRowWords * sizeof(uint32_t), 0,
+                              (size_t)a.K * sizeof(uint32_t), a.B,
+                              stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   for (int k = 0; k < a.K; ++k) {
     dspark_status st = timed_launch(
         t, 0, stream, tc ? launch_position_tc : launch_position_generic, a, k,
@@ -226,7 +232,7 @@ dspark_status dspark_draft_block(
     const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
     int32_t* tokens, float* logits, float* draft_probs, void* workspace,
     size_t workspace_bytes, cudaStream_t stream) {
-  DraftArgs a;
+  DraftArgs a{};
   dspark_status st = prepare_draft(
       base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
       pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
@@ -244,7 +250,7 @@ dspark_status dspark_draft_block_profile(
     size_t workspace_bytes, float* stage_ms, int* stage_launches,
     cudaStream_t stream) {
   if (!stage_ms || !stage_launches) return DSPARK_ERR_INVALID_ARG;
-  DraftArgs a;
+  DraftArgs a{};
   dspark_status st = prepare_draft(
       base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
       pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
@@ -281,7 +287,7 @@ dspark_status dspark_draft_block_noalloc(
     const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
     int32_t* tokens, float* logits, float* draft_probs, cudaStream_t stream) {
   // host-side checks first, against a stand-in scratch address
-  DraftArgs a;
+  DraftArgs a{};
   void* const stand_in = reinterpret_cast<void*>(uintptr_t(256));
   dspark_status st = prepare_draft(
       base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,

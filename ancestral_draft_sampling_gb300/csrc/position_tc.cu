@@ -18,20 +18,26 @@
 //                   tcgen05.mma kind::f16 (M = 128 vocab rows, N = B rounded
 //                   up to 16, K = r) into one of two TMEM accumulators.  A
 //                   (the Wb tile) is vocab-major, B (u) is r-major.
-//   warps 2..17     compute.  Warp (q, j), q = warp % 4, drains TMEM lanes
-//                   32q.. (vocab) of column group j (requests j*B/4 ..) and
-//                   writes l = base + bias (l = bias on padding rows) into
-//                   the tile buffer, in place.  After one barrier the tile
-//                   holds the float32 biased logits: one thread stores it to
-//                   global memory with a TMA tile store, and warp w takes
-//                   requests w, w+16, ... with lane L on vocab 4L .. 4L+3
-//                   (one Philox block): scaled logits, noise, the decision
-//                   and the sum-exp, all from shared memory.
+//   warps 2..25     compute.  Warp (q, j), q = warp % 4, drains TMEM lanes
+//                   32q.. (vocab) of column group j (one sixth of the
+//                   requests) and writes l = base + bias (l = bias on padding
+//                   rows) into the tile buffer, in place.  After one barrier
+//                   the tile holds the float32 biased logits: one thread
+//                   stores it to global memory with a TMA tile store, and
+//                   compute warp w takes requests w, w+24, ... with lane L on
+//                   vocab 4L .. 4L+3 (one Philox block): scaled logits,
+//                   noise, the decision and the sum-exp, all from shared
+//                   memory.
 // Decision: a conservative test per entry (one exp2, no logarithm) admits
-// every entry that may beat the request's best score so far; only those get
-// the exact score s + g, merged over the warp by a butterfly.  The same
-// exp2 value, exp(s - best), feeds the sum-exp: the best score is the
-// reference of each request's running sum.
+// every entry that may beat a reference score; only those get the exact
+// score s + g, merged over the warp by max/min reductions.  The reference
+// is the larger of the request's best score in this CTA and the best score
+// any CTA has posted for the request so far (an atomic maximum in global
+// memory, read once per tile): a score some entry reaches, so an entry
+// below it cannot win.  The same exp2 values, exp(s - reference), feed the
+// sum-exp, which is kept relative to the reference.  The Philox rounds
+// that depend only on the request's key and counter words are folded into
+// per-request constants.
 //
 // Every mbarrier wait is bounded; on a timeout the kernel records an error
 // in the workspace control word, stops issuing work, waits (bounded) for
@@ -52,11 +58,16 @@ constexpr int kTileV = 128;                        // vocab rows per tile (M)
 constexpr int kKChunk = 64;                        // r per pipeline stage
 constexpr int kBoxBytes = 64 * kKChunk * 2;        // one 64x64 bf16 box
 constexpr int kStageBytes = 2 * kBoxBytes;         // 128 vocab x 64 r
-constexpr int kComputeWarps = 16;
+constexpr int kComputeWarps = 24;
 constexpr int kThreads = 32 * (2 + kComputeWarps);
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kMaxBpad = 96;
-constexpr int kMaxRows = kMaxBpad / kComputeWarps; // requests per warp
+constexpr int kColGroups = kComputeWarps / 4;
+constexpr int kMaxGcols = (kMaxBpad / kColGroups + 3) / 4 * 4;
+constexpr int kMaxRows = kMaxGcols / 4;
+__host__ __device__ constexpr int group_cols(int bpad) {
+  return ((bpad + kColGroups - 1) / kColGroups + 3) / 4 * 4;
+}
 constexpr uint32_t kTmemCols = 256;                // two accumulators
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSpin = 1u << 22;
@@ -75,10 +86,11 @@ constexpr float kSumScale = 2.3275186e-10f;
 // Per-request constants in shared memory.  The Philox round keys of the
 // request's key (seed) are precomputed, so a noise block costs the ten
 // rounds' multiplies and XORs only.
-struct RowConst {
-  uint32_t rk[20];    // round r uses (rk[2r], rk[2r+1]) = key + r * (W0, W1)
-  uint32_t c1, c2, c3;  // counter words 1..3: k | stream << 16, offset lo, hi
-  uint32_t flags;     // bit 0: padding row, bit 1: greedy request
+struct alignas(16) RowConst {
+  uint4 pre;     // rounds 1-2 folded: (C1, D2, E2, F2), see row_noise
+  uint4 rk[4];   // round keys of rounds 3..10: rk[j] = rounds 2j+3, 2j+4
+  uint32_t flags;  // bit 0: padding row, bit 1: greedy request
+  uint32_t pad[3];
 };
 constexpr uint32_t kRowPad = 1u, kRowGreedy = 2u;
 
@@ -103,12 +115,14 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 }
 
 // Running state of one request in the compute warp that owns it:
-//   sum        per lane: sum of exp(s - best) over the lane's entries;
-//   best, idx  the same in every lane: the largest decision score so far
-//              (s + g for a sampled request, s for a greedy one) and its
-//              lowest vocab index (kNoIndex while nothing has won).
+//   sum        per lane: sum of exp(s - ref) over the lane's entries;
+//   best, idx  the same in every lane: the largest decision score in this
+//              CTA so far (s + g for a sampled request, s for a greedy one)
+//              and its lowest vocab index (kNoIndex while nothing has won);
+//   ref        the same in every lane: the reference of the candidate test
+//              and the sum, max(best, posted hints) (-inf at first).
 struct RowState {
-  float sum, best;
+  float sum, best, ref;
   int idx;
 };
 
@@ -179,21 +193,56 @@ __device__ __forceinline__ void warp_take_best(RowState& st, float cb, int ci) {
   }
 }
 
-// Philox4x32-10 block with precomputed round keys (same function as
-// philox4x32_10: the published multipliers; key + r * Weyl constants).
-__device__ __forceinline__ uint4 philox_rk(uint4 c, const uint32_t* rk) {
+// One Philox4x32-10 round (the published multipliers) with round key k.
+__device__ __forceinline__ uint4 philox_round(uint4 c, uint32_t k0, uint32_t k1) {
+  const unsigned long long pa = (unsigned long long)0xD2511F53u * c.x;
+  const unsigned long long pb = (unsigned long long)0xCD9E8D57u * c.z;
+  return make_uint4((uint32_t)(pb >> 32) ^ c.y ^ k0, (uint32_t)pb,
+                    (uint32_t)(pa >> 32) ^ c.w ^ k1, (uint32_t)pa);
+}
+
+// The noise block of vocab v: Philox4x32-10 of counter (v >> 2, c1, c2, c3)
+// under the request's key.  Only counter word 0 varies along a row, so the
+// parts of rounds 1 and 2 that depend on the other words alone are
+// per-request constants (row_constants): round 1 gives
+// (A, B, hi(M0 x0) ^ C1, lo(M0 x0)) with A = hi(M1 c2) ^ c1 ^ k0,
+// B = lo(M1 c2), C1 = c3 ^ k1; round 2 then gives
+// (hi(M1 z) ^ D2, lo(M1 z), lo(M0 x0) ^ E2, F2) with z the third word,
+// D2 = B ^ k0', E2 = hi(M0 A) ^ k1', F2 = lo(M0 A).
+__device__ __forceinline__ uint4 row_noise(const RowConst& rc, int v) {
+  const uint4 pre = rc.pre;
+  const unsigned long long pa = (unsigned long long)0xD2511F53u * ((uint32_t)v >> 2);
+  const uint32_t z = (uint32_t)(pa >> 32) ^ pre.x;
+  const unsigned long long pb = (unsigned long long)0xCD9E8D57u * z;
+  uint4 c = make_uint4((uint32_t)(pb >> 32) ^ pre.y, (uint32_t)pb,
+                       (uint32_t)pa ^ pre.z, pre.w);
 #pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const unsigned long long pa = (unsigned long long)0xD2511F53u * c.x;
-    const unsigned long long pb = (unsigned long long)0xCD9E8D57u * c.z;
-    c = make_uint4((uint32_t)(pb >> 32) ^ c.y ^ rk[2 * r], (uint32_t)pb,
-                   (uint32_t)(pa >> 32) ^ c.w ^ rk[2 * r + 1], (uint32_t)pa);
+  for (int j = 0; j < 4; ++j) {
+    const uint4 k = rc.rk[j];
+    c = philox_round(c, k.x, k.y);
+    c = philox_round(c, k.z, k.w);
   }
   return c;
 }
 
-__device__ __forceinline__ uint4 row_noise(const RowConst& rc, int v) {
-  return philox_rk(make_uint4((uint32_t)v >> 2, rc.c1, rc.c2, rc.c3), rc.rk);
+// Per-request constants of row_noise for key (k0, k1) and counter words
+// c1, c2, c3 (round r uses key (k0 + r W0, k1 + r W1), r = 0..9).
+__device__ __forceinline__ void row_constants(RowConst& rc, uint32_t k0,
+                                              uint32_t k1, uint32_t c1,
+                                              uint32_t c2, uint32_t c3) {
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  const unsigned long long m1c2 = (unsigned long long)0xCD9E8D57u * c2;
+  const uint32_t A = (uint32_t)(m1c2 >> 32) ^ c1 ^ k0;
+  const uint32_t Bv = (uint32_t)m1c2;
+  const uint32_t C1 = c3 ^ k1;
+  const unsigned long long m0a = (unsigned long long)0xD2511F53u * A;
+  rc.pre = make_uint4(C1, Bv ^ (k0 + W0), (uint32_t)(m0a >> 32) ^ (k1 + W1),
+                      (uint32_t)m0a);
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t r = 2 * j + 2;
+    rc.rk[j] = make_uint4(k0 + r * W0, k1 + r * W1, k0 + (r + 1) * W0,
+                          k1 + (r + 1) * W1);
+  }
 }
 
 // Exact decision scores of the sampled entries in `cand`, merged into st.
@@ -217,20 +266,31 @@ __device__ __forceinline__ void decide_sampled(RowState& st, uint32_t cand,
 
 // The sum-exp of four entries relative to the request's best (after the
 // decision): f = 2^(32+slack) exp(s - best) are the candidate-test values.
-__device__ __forceinline__ void add_sum(RowState& st, float old_best,
+__device__ __forceinline__ void add_sum(RowState& st, float old_ref,
                                         const float (&s)[4], float (&f)[4]) {
-  if (st.best != old_best) {  // new reference (the same in every lane)
-    if (old_best != -INFINITY) st.sum *= ex2_approx((old_best - st.best) * kLog2e);
-    const float tc = thr_const(st.best);
+  if (st.best > st.ref) st.ref = st.best;
+  if (st.ref != old_ref) {  // new reference (the same in every lane)
+    if (old_ref != -INFINITY) st.sum *= ex2_approx((old_ref - st.ref) * kLog2e);
+    const float tc = thr_const(st.ref);
 #pragma unroll
     for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
   }
-  if (st.best == -INFINITY) {  // nothing has won: only NaN poisons the sum
+  if (st.ref == -INFINITY) {  // nothing has won: only NaN poisons the sum
     if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3]))
       st.sum = __int_as_float(0x7fc00000);
   } else {
     st.sum = fmaf(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
                   kSumScale, st.sum);
+  }
+}
+
+// A best score posted by another CTA (order-preserving bits, 0 = none)
+// raises the reference of the candidate test and of the sum.
+__device__ __forceinline__ void adopt_hint(RowState& st, uint32_t h) {
+  if (h > ordered_bits(st.ref)) {
+    const float r = from_ordered_bits(h);
+    if (st.ref != -INFINITY) st.sum *= ex2_approx((st.ref - r) * kLog2e);
+    st.ref = r;
   }
 }
 
@@ -240,8 +300,8 @@ __device__ __forceinline__ void sampled_step(const RowConst& rc,
                                              const float (&s)[4], int v,
                                              RowState& st) {
   const uint4 w = row_noise(rc, v);
-  const float old_best = st.best;
-  const float tc = thr_const(old_best);
+  const float old_ref = st.ref;
+  const float tc = thr_const(old_ref);
   float f[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
@@ -250,7 +310,7 @@ __device__ __forceinline__ void sampled_step(const RowConst& rc,
                         (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
                         (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
   if (__any_sync(0xffffffffu, cand != 0u)) decide_sampled(st, cand, s, w, v);
-  add_sum(st, old_best, s, f);
+  add_sum(st, old_ref, s, f);
 }
 
 // Approximate decision score s - log E, used only to choose which entry of
@@ -313,10 +373,10 @@ __device__ __forceinline__ void greedy_step(const float (&s)[4], int v,
     warp_take_best(st, cb, ci);
   }
   float f[4];
-  const float tc = thr_const(st.best);
+  const float tc = thr_const(st.ref);
 #pragma unroll
   for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
-  add_sum(st, st.best, s, f);
+  add_sum(st, st.ref, s, f);
 }
 
 template <bool kUnitT>
@@ -418,24 +478,19 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     }
     for (int b = ct; b < P.bpad; b += kComputeThreads) {
       RowConst rc;
-      uint32_t k0 = 0, k1 = 0;
-      rc.c1 = (uint32_t)P.k | ((uint32_t)kNoiseDraft << 16);
-      rc.c2 = rc.c3 = 0;
+      uint32_t k0 = 0, k1 = 0, c2 = 0, c3 = 0;
       rc.flags = 0;
+      rc.pad[0] = rc.pad[1] = rc.pad[2] = 0;
       if (b < a.B) {
         k0 = (uint32_t)a.seed[b];
         k1 = (uint32_t)(a.seed[b] >> 32);
-        rc.c2 = (uint32_t)a.offset[b];
-        rc.c3 = (uint32_t)(a.offset[b] >> 32);
+        c2 = (uint32_t)a.offset[b];
+        c3 = (uint32_t)(a.offset[b] >> 32);
         rc.flags = (a.pad_row != nullptr && a.pad_row[b] != 0 ? kRowPad : 0u) |
                    (a.greedy != nullptr && a.greedy[b] != 0 ? kRowGreedy : 0u);
       }
-      for (int r = 0; r < 10; ++r) {
-        rc.rk[2 * r] = k0;
-        rc.rk[2 * r + 1] = k1;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
-      }
+      row_constants(rc, k0, k1, (uint32_t)P.k | ((uint32_t)kNoiseDraft << 16),
+                    c2, c3);
       rows[b] = rc;
     }
     fence_proxy_async_smem();
@@ -554,13 +609,26 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     // ----------------------------------------------------------- compute
     const int cw = warp - 2;
     const int q = warp & 3;                  // TMEM lane quarter
-    const int gcols = P.bpad / 4;            // drained columns (requests)
+    const int gcols = group_cols(P.bpad);
     const int col0 = (cw >> 2) * gcols;
     const int m = 32 * q + lane;             // drained vocab row of the tile
-    const int rpw = P.bpad / kComputeWarps;  // requests per warp
     const bool storer = cw == 0 && lane == 0;
+    // lane i < kMaxRows: the best-score hint of this warp's row i (sampled
+    // requests only)
+    uint32_t* hint_ptr = nullptr;
+    {
+      const int hb = cw + kComputeWarps * lane;
+      if (lane < kMaxRows && hb < a.B && !(rows[hb].flags & kRowGreedy))
+        hint_ptr = a.hints + (size_t)hb * kHintRowWords + P.k;
+    }
     // drained columns that hold requests (< B), and which are padding rows
     const int nvalid = a.B - col0 < 0 ? 0 : (a.B - col0 < gcols ? a.B - col0 : gcols);
+    uint32_t greedy_mask = 0;  // bit i: this warp's row i is greedy
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+      const int b = cw + kComputeWarps * i;
+      if (b < a.B && (rows[b].flags & kRowGreedy)) greedy_mask |= 1u << i;
+    }
     uint32_t padmask = 0;
     for (int c = 0; c < nvalid; ++c)
       padmask |= ((rows[col0 + c].flags & kRowPad) ? 1u : 0u) << c;
@@ -571,6 +639,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int i = 0; i < kMaxRows; ++i) {
       st[i].sum = 0.0f;
       st[i].best = -INFINITY;  // nothing to beat yet
+      st[i].ref = -INFINITY;
       st[i].idx = kNoIndex;
     }
 
@@ -579,6 +648,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       const uint32_t ph = (uint32_t)(t >> 1) & 1u;
       const int v0 = (t_begin + t) * kTileV;
       float* tile = tiles + (size_t)buf * tile_floats;
+      const uint32_t hint_in = hint_ptr ? __ldcg(hint_ptr) : 0u;
       // drain: l = base + bias for this warp's (vocab row m, request) block
       bool ok = !*abort_flag &&
                 mbar_wait(kStaged ? &base_full[0] : &base_full[buf],
@@ -589,9 +659,9 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         tc_fence_after();
         const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
                                (uint32_t)buf * kAccCols + (uint32_t)col0;
-        float bias[kMaxBpad / 4];
+        float bias[kMaxGcols];
 #pragma unroll
-        for (int c = 0; c < kMaxBpad / 4; c += 4)
+        for (int c = 0; c < kMaxGcols; c += 4)
           if (c < gcols) {
             float q4[4];
             tmem_ld4(taddr + (uint32_t)c, q4);
@@ -603,7 +673,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         tmem_ld_wait();
         float* col = tile + col0 * kTileV + m;
 #pragma unroll
-        for (int c = 0; c < kMaxBpad / 4; ++c) {
+        for (int c = 0; c < kMaxGcols; ++c) {
           if (c >= nvalid) break;
           float x;
           if (kStaged)
@@ -630,20 +700,31 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         const bool valid = v < V;  // V % 8 == 0: v..v+3 all in range
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
-          if (i >= rpw) break;
           const int b = cw + kComputeWarps * i;
           if (b >= a.B) break;
           const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
           float sv[4];
           scaled4<kUnitT>(l4, valid, T, sv);
           const RowConst& rc = rows[b];
-          if (rc.flags & kRowGreedy)
+          const uint32_t h = __shfl_sync(0xffffffffu, hint_in, i);
+          if ((greedy_mask >> i) & 1u) {
             greedy_step(sv, v, st[i]);
-          else if (st[i].best == -INFINITY)
-            sampled_first(rc, sv, v, st[i]);
-          else
-            sampled_step(rc, sv, v, st[i]);
+          } else {
+            adopt_hint(st[i], h);
+            // first tile: bootstrap the reference; afterwards the steady
+            // state (which also handles a reference still at -inf)
+            if (t == 0 && st[i].ref == -INFINITY)
+              sampled_first(rc, sv, v, st[i]);
+            else
+              sampled_step(rc, sv, v, st[i]);
+          }
         }
+        // post bests that beat the hint read for this tile
+        uint32_t mine = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxRows; ++i)
+          if (lane == i && st[i].idx != kNoIndex) mine = ordered_bits(st[i].best);
+        if (hint_ptr && mine > hint_in) atomicMax(hint_ptr, mine);
       }
       if (storer) bulk_wait_read_all();  // the store has read the tile
       mbar_arrive(&tile_free[buf]);
@@ -653,7 +734,6 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     // lanes' sums (same reference) added by a butterfly
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
-      if (i >= rpw) break;
       const int b = cw + kComputeWarps * i;
       if (b >= a.B) break;
       float sum = st[i].sum;
@@ -664,7 +744,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         ChunkStat cs;
         cs.best = st[i].best;
         cs.idx = st[i].idx;
-        cs.m = st[i].best;  // the reference of the sum (-inf: nothing won)
+        cs.m = st[i].ref;  // the reference of the sum (-inf: nothing won)
         cs.s = sum;
         a.stats[(size_t)b * kMaxChunks + chunk] = cs;
       }

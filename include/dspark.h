@@ -79,8 +79,8 @@ typedef enum {
 /*
  * Bytes of device workspace dspark_draft_block needs for these sizes
  * (0 if the sizes are unsupported).  The workspace holds per-chunk softmax
- * statistics, per-row (max, sum-exp) of every position, and a device error
- * word.  Its contents need not be initialised and are overwritten by each
+ * statistics, per-row (max, sum-exp) of every position, the best-score hints
+ * the position kernels share across CTAs, and a device error word.  Its contents need not be initialised and are overwritten by each
  * call; two calls in flight at the same time must not share a workspace.
  */
 DSPARK_API size_t dspark_draft_workspace_bytes(int B, int K, int V, int r);
