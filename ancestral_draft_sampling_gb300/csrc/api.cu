@@ -133,6 +133,19 @@ dspark_status timed_launch(StageTimer* t, int cls, cudaStream_t stream,
   return DSPARK_OK;
 }
 
+// The pick after a tensor-core position overlaps that kernel's end (both
+// are launched for programmatic dependent launch); after the FFMA kernel it
+// is an ordinary launch.
+cudaError_t launch_pick_overlapped(const DraftArgs& a, int k, int n,
+                                   cudaStream_t s) {
+  return launch_pick(a, k, n, true, s);
+}
+
+cudaError_t launch_pick_plain(const DraftArgs& a, int k, int n,
+                              cudaStream_t s) {
+  return launch_pick(a, k, n, false, s);
+}
+
 cudaError_t proposals_adapter(const DraftArgs& a, int, int, cudaStream_t s) {
   return launch_proposals(a, s);
 }
@@ -159,7 +172,7 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   // merges them in slot order
   const int want = tc ? position_tc_chunks(a.V, sms) : sms;
   const int n_chunks = tc ? want : generic_chunks_used(a.V, want);
-  // the cross-CTA best-score hints of every position start empty
+  // the cross-CTA best-score hints of every position start at zero
   if (tc && cudaMemset2DAsync(a.hints, kHintRowWords * sizeof(uint32_t), 0,
                               (size_t)a.K * sizeof(uint32_t), a.B,
                               stream) != cudaSuccess)
@@ -169,7 +182,8 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
         t, 0, stream, tc ? launch_position_tc : launch_position_generic, a, k,
         want);
     if (st != DSPARK_OK) return st;
-    st = timed_launch(t, 1, stream, launch_pick, a, k, n_chunks);
+    st = timed_launch(t, 1, stream, tc ? launch_pick_overlapped : launch_pick_plain,
+                      a, k, n_chunks);
     if (st != DSPARK_OK) return st;
   }
   return timed_launch(t, 2, stream, proposals_adapter, a, 0, 0);

@@ -244,8 +244,10 @@ bool position_tc_supported(const DraftArgs& a);
 int position_tc_chunks(int V, int sm_count);
 cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
                                cudaStream_t stream);
+// overlap_previous: launched with programmatic stream serialisation (the
+// kernel waits for the previous grid before reading its statistics).
 cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
-                        cudaStream_t stream);
+                        bool overlap_previous, cudaStream_t stream);
 cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream);
 cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           const uint64_t* seed, const uint64_t* offset, int B,

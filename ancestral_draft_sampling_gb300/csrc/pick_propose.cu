@@ -1,40 +1,38 @@
 // pick_propose.cu -- the cross-chunk pick and the post-block proposal writer.
 //
 // brb-nv/TensorRT-LLM PR #27, "2. One fused kernel per draft position":
-// "a small kernel picks the token" from the per-chunk statistics, and after
+// a small kernel picks the token from the per-chunk statistics, and after
 // the block one kernel writes q_k = softmax(logits_k / T) for every position
 // from the float32 biased logits, recomputing logits_k / T bit for bit as the
 // draw used it.  Greedy requests store a one-hot proposal (PR #27, Test
 // Coverage, "Also checked").
 #include "dspark_common.cuh"
+#include "sm100_ptx.cuh"
 
 namespace dspark {
 namespace {
 
-constexpr int kPickThreads = 256;
+constexpr int kPickThreads = 32;
 
-// One CTA per request: merge the chunk statistics of position k in a fixed
-// order, write d_k and the row's (M, S).
+// One warp per request: merge the chunk statistics of position k (lane l
+// takes chunks l, l+32, ... in order, then a butterfly across the lanes),
+// write d_k and the row's (M, S).  When launched for programmatic dependent
+// launch it lets the next position's kernel be scheduled at once and waits
+// for the position kernel before reading its statistics.
 __global__ void __launch_bounds__(kPickThreads)
 pick_kernel(DraftArgs a, int k, int n_chunks) {
-  __shared__ ChunkStat part[kPickThreads / 32];
+  sm100::launch_dependents();
+  sm100::grid_dependency_wait();
   const int b = blockIdx.x;
   ChunkStat st = empty_stat();
   for (int c = threadIdx.x; c < n_chunks; c += kPickThreads)
     merge_stat(st, a.stats[(size_t)b * kMaxChunks + c]);
   st = warp_reduce_stat(st);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) part[warp] = st;
-  __syncthreads();
-  if (warp == 0) {
-    st = lane < kPickThreads / 32 ? part[lane] : empty_stat();
-    st = warp_reduce_stat(st);
-    if (lane == 0) {
-      const size_t row = (size_t)b * a.K + k;
-      a.tokens[row] = (st.idx == kNoIndex) ? 0 : st.idx;
-      a.rowstats[2 * row] = st.m;
-      a.rowstats[2 * row + 1] = st.s;
-    }
+  if (threadIdx.x == 0) {
+    const size_t row = (size_t)b * a.K + k;
+    a.tokens[row] = (st.idx == kNoIndex) ? 0 : st.idx;
+    a.rowstats[2 * row] = st.m;
+    a.rowstats[2 * row + 1] = st.s;
   }
 }
 
@@ -105,9 +103,18 @@ __global__ void noise_words_kernel(uint64_t seed, uint64_t offset, int k,
 }  // namespace
 
 cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
-                        cudaStream_t stream) {
-  pick_kernel<<<a.B, kPickThreads, 0, stream>>>(a, k, n_chunks);
-  return cudaGetLastError();
+                        bool overlap_previous, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.B, 1, 1);
+  cfg.blockDim = dim3(kPickThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, pick_kernel, a, k, n_chunks);
 }
 
 cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream) {

@@ -412,7 +412,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   uint64_t* tile_free = base_full + 2;
   uint64_t* stage_free = tile_free + 2;
   uint64_t* mma_done = stage_free + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* u_ready = mma_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(u_ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const DraftArgs& a = P.a;
@@ -443,6 +444,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     }
     mbar_init(stage_free, kComputeThreads);
     mbar_init(mma_done, 1);
+    mbar_init(u_ready, kComputeThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -456,26 +458,9 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     tmem_relinquish();
   }
   if (warp >= 2) {
-    // u row b = U[d_{k-1}(b)], stored r-major with the 128-byte swizzle: row
-    // b of r-chunk c at c*(bpad*128) + b*128, 16-byte piece p at (p ^ (b & 7))
+    // per-request constants (inputs only: they may be read before the
+    // previous position's kernel has finished)
     const int ct = threadIdx.x - 64;
-    const int pieces = a.r / 8;
-    const uint16_t* U = static_cast<const uint16_t*>(a.U);
-    for (int i = ct; i < P.bpad * pieces; i += kComputeThreads) {
-      const int b = i / pieces, piece = i - b * pieces;
-      const int c = piece >> 3, p = piece & 7;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (b < a.B) {
-        int prev = (P.k == 0) ? a.d0[b] : a.tokens[(size_t)b * a.K + (P.k - 1)];
-        if ((unsigned)prev >= (unsigned)a.V) {
-          if (piece == 0) a.control[0] = kDevErrBadToken;
-          prev = 0;
-        }
-        val = __ldg(reinterpret_cast<const uint4*>(U + (size_t)prev * a.r) + piece);
-      }
-      *reinterpret_cast<uint4*>(u_s + (size_t)c * (P.bpad * 128) + b * 128 +
-                                ((p ^ (b & 7)) << 4)) = val;
-    }
     for (int b = ct; b < P.bpad; b += kComputeThreads) {
       RowConst rc;
       uint32_t k0 = 0, k1 = 0, c2 = 0, c3 = 0;
@@ -493,11 +478,13 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
                     c2, c3);
       rows[b] = rc;
     }
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // the pick kernel that follows may be scheduled now; it waits for this
+  // grid to finish before it reads the statistics
+  if (threadIdx.x == 0) launch_dependents();
   const uint32_t tmem_base = *tmem_holder;
 
   if (warp == 0) {
@@ -562,6 +549,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTileV, (uint32_t)P.bpad, 1u, 0u);
       const uint32_t u_base = smem_u32(u_s);
+      if (!mbar_wait(u_ready, 0u, kSpin)) fail(kDevErrTimeout);
       int g = 0;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t) {
         const int acc = t & 1;
@@ -607,6 +595,32 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     __syncwarp();
   } else {
     // ----------------------------------------------------------- compute
+    // u row b = U[d_{k-1}(b)], stored r-major with the 128-byte swizzle: row
+    // b of r-chunk c at c*(bpad*128) + b*128, 16-byte piece p at (p ^ (b & 7)).
+    // d_{k-1} comes from the previous position's kernel: wait for it first.
+    grid_dependency_wait();
+    {
+    const int ct = threadIdx.x - 64;
+    const int pieces = a.r / 8;
+    const uint16_t* U = static_cast<const uint16_t*>(a.U);
+    for (int i = ct; i < P.bpad * pieces; i += kComputeThreads) {
+      const int b = i / pieces, piece = i - b * pieces;
+      const int c = piece >> 3, p = piece & 7;
+      uint4 val = make_uint4(0u, 0u, 0u, 0u);
+      if (b < a.B) {
+        int prev = (P.k == 0) ? a.d0[b] : a.tokens[(size_t)b * a.K + (P.k - 1)];
+        if ((unsigned)prev >= (unsigned)a.V) {
+          if (piece == 0) a.control[0] = kDevErrBadToken;
+          prev = 0;
+        }
+        val = __ldg(reinterpret_cast<const uint4*>(U + (size_t)prev * a.r) + piece);
+      }
+      *reinterpret_cast<uint4*>(u_s + (size_t)c * (P.bpad * 128) + b * 128 +
+                                ((p ^ (b & 7)) << 4)) = val;
+    }
+    }
+    fence_proxy_async_smem();  // the MMA reads u through the async proxy
+    mbar_arrive(u_ready);
     const int cw = warp - 2;
     const int q = warp & 3;                  // TMEM lane quarter
     const int gcols = group_cols(P.bpad);
@@ -790,7 +804,7 @@ Layout make_layout(int B, int r, int base_elt) {
   const size_t tiles = 2 * (size_t)L.bpad * kTileV * 4;
   const size_t stage = base_elt == 2 ? (size_t)L.bpad * kTileV * 2 : 0;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowConst), 16);
-  const size_t bars = (2 * kMaxStages + 10) * 8 + 16;
+  const size_t bars = (2 * kMaxStages + 11) * 8 + 16;
   const size_t fixed = u + tiles + stage + rows + bars + 1024;
   L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
   if (L.stages > kMaxStages) L.stages = kMaxStages;
@@ -820,16 +834,30 @@ CUresult encode_position_map(CUtensorMap* map, CUtensorMapDataType dt,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Positions after the first are launched with programmatic stream
+// serialisation behind the previous position's pick kernel: their set-up
+// and first Wb / drafter-logit loads overlap the end of the previous
+// position; they wait for its token before the gather.
 template <typename BT, bool kUnitT>
 cudaError_t launch_typed(const CUtensorMap& wb, const CUtensorMap& bm,
                          const CUtensorMap& om, const TcParams& P, size_t smem,
-                         int n_chunks, cudaStream_t stream) {
+                         int n_chunks, bool overlap_previous,
+                         cudaStream_t stream) {
   auto kern = position_tc_kernel<BT, kUnitT>;
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  kern<<<n_chunks, kThreads, smem, stream>>>(wb, bm, om, P);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)n_chunks, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap_previous ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, wb, bm, om, P);
 }
 
 }  // namespace
@@ -887,11 +915,12 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
   P.rows_off = L.rows_off;
   P.bar_off = L.bar_off;
   const bool unit = a.T == 1.0f;
+  const bool pdl = k > 0;
   if (elt == 4)
-    return unit ? launch_typed<float, true>(wb, bm, om, P, L.smem, n_chunks, stream)
-                : launch_typed<float, false>(wb, bm, om, P, L.smem, n_chunks, stream);
-  return unit ? launch_typed<uint16_t, true>(wb, bm, om, P, L.smem, n_chunks, stream)
-              : launch_typed<uint16_t, false>(wb, bm, om, P, L.smem, n_chunks, stream);
+    return unit ? launch_typed<float, true>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
+                : launch_typed<float, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream);
+  return unit ? launch_typed<uint16_t, true>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
+              : launch_typed<uint16_t, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream);
 }
 
 }  // namespace dspark

@@ -72,6 +72,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   return false;
 }
 
+// ------------------------------------------------- programmatic launch
+// Blocks until every grid this one depends on (the previous kernel in the
+// stream, when launched with programmatic stream serialisation) has
+// completed and its memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the dependent grid be scheduled before this one completes.
+__device__ __forceinline__ void launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map,
                                             uint64_t* bar, int x, int y) {

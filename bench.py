@@ -326,7 +326,8 @@ def run_ours(args, rank, world):
 
     # per-kernel durations, CUDA events around every launch on its stream
     prof = {"position": [0.0, 0], "pick": [0.0, 0], "proposal": [0.0, 0]}
-    for _ in range(max(3, min(args.steps, 10))):
+    prof_reps = max(3, min(args.steps, 10))
+    for _ in range(prof_reps):
         p = pkg.draft_block_profile(dev["base"], dev["U"], dev["Wb"], dev["d0"],
                                     dev["seed"], dev["offset"], w.T,
                                     greedy=dev["greedy"], pad_row=dev["pad_row"],
@@ -431,7 +432,8 @@ def run_ours(args, rank, world):
             "roofline": roofline,
             "clocks": clocks.summary(),
             "verify": verify,
-            "gpu_launches": args.steps * (2 * K + 1),
+            # kernels of one block (counted by the profile pass) x steps
+            "gpu_launches": args.steps * sum(v[1] for v in prof.values()) // prof_reps,
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "path": "pinned host -> device copies, dspark_draft_block, "
