@@ -37,13 +37,15 @@ pick_kernel(DraftArgs a, int k, int n_chunks) {
 }
 
 constexpr int kPropThreads = 256;
-constexpr int kPropPerThread = 8;  // two float4 per thread per row segment
+constexpr int kPropN4 = 4;  // float4 per thread (2 and 8 measured slower)
+constexpr int kPropPerThread = 4 * kPropN4;
 
 __device__ __forceinline__ float scale(float l, float T) {
   return T == 1.0f ? l : __fdiv_rn(l, T);
 }
 
-// grid = (B*K rows, segments of a row).  q = exp(s - M) * (1 / S).
+// grid = (B*K rows, segments of a row).  q = exp(s - M) * (1 / S).  Every
+// load of a thread is issued before its first store.
 template <bool kVec>
 __global__ void __launch_bounds__(kPropThreads)
 proposals_kernel(DraftArgs a) {
@@ -54,25 +56,30 @@ proposals_kernel(DraftArgs a) {
   const float invS = __frcp_rn(a.rowstats[2 * (size_t)row + 1]);
   const bool greedy = a.greedy != nullptr && a.greedy[b] != 0;
   const int token = greedy ? a.tokens[row] : -1;
-  const float* lrow = a.logits + (size_t)row * V;
-  float* qrow = a.probs + (size_t)row * V;
+  const float* __restrict__ lrow = a.logits + (size_t)row * V;
+  float* __restrict__ qrow = a.probs + (size_t)row * V;
   const float T = a.T;
   const int seg = kPropThreads * kPropPerThread;
   const int v_begin = blockIdx.y * seg;
   if (kVec) {
+    float4 l[kPropN4];
 #pragma unroll
-    for (int i = 0; i < kPropPerThread / 4; ++i) {
+    for (int i = 0; i < kPropN4; ++i) {
+      const int v = v_begin + (i * kPropThreads + threadIdx.x) * 4;
+      if (v < V) l[i] = __ldcs(reinterpret_cast<const float4*>(lrow + v));
+    }
+#pragma unroll
+    for (int i = 0; i < kPropN4; ++i) {
       const int v = v_begin + (i * kPropThreads + threadIdx.x) * 4;
       if (v >= V) break;  // V % 4 == 0: the whole float4 is in range
-      const float4 l = __ldcs(reinterpret_cast<const float4*>(lrow + v));
       float4 q;
       if (greedy) {
         q = make_float4(v == token, v + 1 == token, v + 2 == token, v + 3 == token);
       } else {
-        q.x = __fmul_rn(expf(scale(l.x, T) - M), invS);
-        q.y = __fmul_rn(expf(scale(l.y, T) - M), invS);
-        q.z = __fmul_rn(expf(scale(l.z, T) - M), invS);
-        q.w = __fmul_rn(expf(scale(l.w, T) - M), invS);
+        q.x = __fmul_rn(expf(scale(l[i].x, T) - M), invS);
+        q.y = __fmul_rn(expf(scale(l[i].y, T) - M), invS);
+        q.z = __fmul_rn(expf(scale(l[i].z, T) - M), invS);
+        q.w = __fmul_rn(expf(scale(l[i].w, T) - M), invS);
       }
       __stcs(reinterpret_cast<float4*>(qrow + v), q);
     }
