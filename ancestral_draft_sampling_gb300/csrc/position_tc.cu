@@ -126,10 +126,12 @@ struct RowState {
   int idx;
 };
 
-// The constant of the candidate test: 32 + 2^-11 - best log2(e)
-// (+inf while nothing has won, which admits every finite entry).
-__device__ __forceinline__ float thr_const(float best) {
-  return fmaf(-best, kLog2e, 32.0f + kThrSlack);
+// The constant of the candidate test for reference `ref`:
+// 32 + 2^-11 - ref log2(e).  While nothing has won (ref = -inf) a huge
+// finite constant stands in: every finite entry is then admitted, and a
+// -inf entry adds exp2(-inf) = 0 to the sum.
+__device__ __forceinline__ float thr_const(float ref) {
+  return fmaf(-fmaxf(ref, -0x1p100f), kLog2e, 32.0f + kThrSlack);
 }
 
 // 2^(32 + slack) exp(s - best).  A sampled entry wins only if s + g > best
@@ -264,24 +266,26 @@ __device__ __forceinline__ void decide_sampled(RowState& st, uint32_t cand,
   warp_take_best(st, cb, ci);
 }
 
-// The sum-exp of four entries relative to the request's best (after the
-// decision): f = 2^(32+slack) exp(s - best) are the candidate-test values.
-__device__ __forceinline__ void add_sum(RowState& st, float old_ref,
-                                        const float (&s)[4], float (&f)[4]) {
-  if (st.best > st.ref) st.ref = st.best;
-  if (st.ref != old_ref) {  // new reference (the same in every lane)
-    if (old_ref != -INFINITY) st.sum *= ex2_approx((old_ref - st.ref) * kLog2e);
+// After a decision: a best score above the reference becomes the
+// reference; the sum is rescaled to it (while the reference is -inf the sum
+// is 0, or NaN after a NaN entry) and the four test values are recomputed.
+// Warp-uniform (best and ref are the same in every lane).
+__device__ __forceinline__ void raise_ref(RowState& st, const float (&s)[4],
+                                          float (&f)[4]) {
+  if (st.best > st.ref) {
+    if (st.ref != -INFINITY) st.sum *= ex2_approx((st.ref - st.best) * kLog2e);
+    st.ref = st.best;
     const float tc = thr_const(st.ref);
 #pragma unroll
     for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
   }
-  if (st.ref == -INFINITY) {  // nothing has won: only NaN poisons the sum
-    if (isnan(s[0]) || isnan(s[1]) || isnan(s[2]) || isnan(s[3]))
-      st.sum = __int_as_float(0x7fc00000);
-  } else {
-    st.sum = fmaf(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
-                  kSumScale, st.sum);
-  }
+}
+
+// The sum-exp of four entries relative to the reference: the test values
+// f = 2^(32+slack) exp(s - ref), scaled back.
+__device__ __forceinline__ void accumulate(RowState& st, const float (&f)[4]) {
+  st.sum = fmaf(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
+                kSumScale, st.sum);
 }
 
 // A best score posted by another CTA (order-preserving bits, 0 = none)
@@ -300,8 +304,7 @@ __device__ __forceinline__ void sampled_step(const RowConst& rc,
                                              const float (&s)[4], int v,
                                              RowState& st) {
   const uint4 w = row_noise(rc, v);
-  const float old_ref = st.ref;
-  const float tc = thr_const(old_ref);
+  const float tc = thr_const(st.ref);
   float f[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
@@ -309,8 +312,11 @@ __device__ __forceinline__ void sampled_step(const RowConst& rc,
                         (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
                         (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
                         (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
-  if (__any_sync(0xffffffffu, cand != 0u)) decide_sampled(st, cand, s, w, v);
-  add_sum(st, old_ref, s, f);
+  if (__any_sync(0xffffffffu, cand != 0u)) {
+    decide_sampled(st, cand, s, w, v);
+    raise_ref(st, s, f);
+  }
+  accumulate(st, f);
 }
 
 // Approximate decision score s - log E, used only to choose which entry of
@@ -340,7 +346,10 @@ __device__ __forceinline__ void sampled_first(const RowConst& rc,
     }
   }
   decide_sampled(st, first, s, w, v);
-  const float tc = thr_const(st.best);
+  if (st.best > st.ref) {  // the reference is -inf here: the sum is 0 or NaN
+    st.ref = st.best;
+  }
+  const float tc = thr_const(st.ref);
   float f[4];
   uint32_t cand = 0;
 #pragma unroll
@@ -349,8 +358,11 @@ __device__ __forceinline__ void sampled_first(const RowConst& rc,
     cand |= (__uint2float_rz(word_of(w, e)) < f[e] ? 1u : 0u) << e;
   }
   cand &= ~first;
-  if (__any_sync(0xffffffffu, cand != 0u)) decide_sampled(st, cand, s, w, v);
-  add_sum(st, -INFINITY, s, f);
+  if (__any_sync(0xffffffffu, cand != 0u)) {
+    decide_sampled(st, cand, s, w, v);
+    raise_ref(st, s, f);
+  }
+  accumulate(st, f);
 }
 
 // A greedy request: no noise; an entry is a candidate iff s > best.
@@ -376,16 +388,17 @@ __device__ __forceinline__ void greedy_step(const float (&s)[4], int v,
   const float tc = thr_const(st.ref);
 #pragma unroll
   for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
-  add_sum(st, st.ref, s, f);
+  raise_ref(st, s, f);
+  accumulate(st, f);
 }
 
 template <bool kUnitT>
-__device__ __forceinline__ void scaled4(const float4 l4, bool valid, float T,
+__device__ __forceinline__ void scaled4(const float4 l4, float T,
                                         float (&s)[4]) {
-  s[0] = valid ? scale<kUnitT>(l4.x, T) : -INFINITY;
-  s[1] = valid ? scale<kUnitT>(l4.y, T) : -INFINITY;
-  s[2] = valid ? scale<kUnitT>(l4.z, T) : -INFINITY;
-  s[3] = valid ? scale<kUnitT>(l4.w, T) : -INFINITY;
+  s[0] = scale<kUnitT>(l4.x, T);
+  s[1] = scale<kUnitT>(l4.y, T);
+  s[2] = scale<kUnitT>(l4.z, T);
+  s[3] = scale<kUnitT>(l4.w, T);
 }
 
 template <typename BT, bool kUnitT>
@@ -647,7 +660,6 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int c = 0; c < nvalid; ++c)
       padmask |= ((rows[col0 + c].flags & kRowPad) ? 1u : 0u) << c;
     const float T = a.T;
-    const int V = a.V;
     RowState st[kMaxRows];
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
@@ -697,6 +709,11 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
             x = col[c * kTileV];
           col[c * kTileV] = ((padmask >> c) & 1u) ? bias[c] : __fadd_rn(x, bias[c]);
         }
+        // the ragged last tile: vocab rows past V become -inf, which no
+        // decision admits and the sum ignores (the logits store clips them)
+        if (v0 + kTileV > a.V && v0 + m >= a.V) {
+          for (int c = 0; c < nvalid; ++c) col[c * kTileV] = -INFINITY;
+        }
         tc_fence_before();
       } else if (!*abort_flag) {
         fail(kDevErrTimeout);
@@ -711,14 +728,13 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       }
       if (!*abort_flag) {
         const int v = v0 + 4 * lane;
-        const bool valid = v < V;  // V % 8 == 0: v..v+3 all in range
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
           const int b = cw + kComputeWarps * i;
           if (b >= a.B) break;
           const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
           float sv[4];
-          scaled4<kUnitT>(l4, valid, T, sv);
+          scaled4<kUnitT>(l4, T, sv);
           const RowConst& rc = rows[b];
           const uint32_t h = __shfl_sync(0xffffffffu, hint_in, i);
           if ((greedy_mask >> i) & 1u) {
