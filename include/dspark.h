@@ -158,7 +158,7 @@ DSPARK_API dspark_status dspark_draft_block_profile(
  * array of DSPARK_NOALLOC_SCRATCH_BYTES bytes (2 MiB), held on every GPU
  * that loads the library until the process exits; sizes whose workspace
  * (dspark_draft_workspace_bytes) exceeds it are rejected with
- * DSPARK_ERR_WORKSPACE before any launch (e.g. B <= 127 at K = 7).
+ * DSPARK_ERR_WORKSPACE before any launch (B <= 102 fits at K = 7).
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
  * routine.  The first call on a device looks up the scratch's device
  * address (with that device current); make that first call before any
