@@ -15,9 +15,10 @@ from typing import Optional
 from . import _lib
 from ._lib import BF16, F32, DsparkError  # noqa: F401
 
-__all__ = ["draft_block", "draft_block_noalloc", "draft_block_profile", "verify_standard", "noise_words", "workspace_bytes",
-           "read_device_error", "DraftWorkspace", "DsparkError", "F32", "BF16",
-           "version"]
+__all__ = ["draft_block", "draft_block_noalloc", "draft_block_profile",
+           "draft_block_host", "HostWorkspace", "verify_standard",
+           "noise_words", "workspace_bytes", "read_device_error",
+           "DraftWorkspace", "DsparkError", "F32", "BF16", "version"]
 
 
 def _torch():
@@ -104,6 +105,52 @@ def draft_block(base_logits, U, Wb, d0, seed, offset, T: float, *,
         _stream(stream))
     _lib.check("dspark_draft_block", st)
     return tokens, logits, draft_probs
+
+
+class HostWorkspace:
+    """Device scratch for dspark_draft_block_host, sized for (B, K, V, r)."""
+
+    def __init__(self, B: int, K: int, V: int, r: int, device=None):
+        torch = _torch()
+        n = int(_lib.load().dspark_draft_host_workspace_bytes(B, K, V, r))
+        if n == 0:
+            raise DsparkError("dspark_draft_host_workspace_bytes", 2)
+        self.nbytes = n
+        self.buffer = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def draft_block_host(base_logits_host, U, Wb, d0_host, seed_host,
+                     offset_host, T: float, *, base_dev, logits, draft_probs,
+                     tokens_host=None, greedy_host=None, pad_row_host=None,
+                     workspace: Optional[HostWorkspace] = None, stream=None,
+                     copy_stream=None):
+    """dspark_draft_block_host: inputs in (pinned) host tensors, tokens back
+    to a host tensor; base_dev [B,K,V] receives the drafter logits on the
+    device, copied position by position on ``copy_stream`` while earlier
+    positions compute on ``stream``.  Returns tokens_host."""
+    torch = _torch()
+    B, K, V = base_logits_host.shape
+    r = U.shape[1]
+    if base_logits_host.is_cuda or d0_host.is_cuda:
+        raise ValueError("base_logits_host and the per-request inputs must "
+                         "be host tensors")
+    if tuple(base_dev.shape) != (B, K, V) or base_dev.dtype != base_logits_host.dtype:
+        raise ValueError("base_dev must match base_logits_host")
+    if tokens_host is None:
+        tokens_host = torch.empty((B, K), dtype=torch.int32).pin_memory()
+    if workspace is None:
+        workspace = HostWorkspace(B, K, V, r, device=base_dev.device)
+    if copy_stream is None:
+        raise ValueError("copy_stream is required (a stream other than stream)")
+    st = _lib.load().dspark_draft_block_host(
+        _ptr(base_logits_host), _dtype_code(base_logits_host), _ptr(U),
+        _ptr(Wb), _dtype_code(U), _ptr(d0_host), _ptr(seed_host),
+        _ptr(offset_host), float(T), _ptr(greedy_host), _ptr(pad_row_host),
+        B, K, V, r, _ptr(base_dev), _ptr(tokens_host), _ptr(logits),
+        _ptr(draft_probs), _ptr(workspace.buffer), workspace.nbytes,
+        _stream(stream), copy_stream.cuda_stream)
+    _lib.check("dspark_draft_block_host", st)
+    return tokens_host
 
 
 def draft_block_noalloc(base_logits, U, Wb, d0, seed, offset, T: float, *,

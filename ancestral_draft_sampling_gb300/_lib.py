@@ -30,6 +30,8 @@ EXPORTED = (
     "dspark_draft_block",
     "dspark_draft_block_profile",
     "dspark_draft_block_noalloc",
+    "dspark_draft_host_workspace_bytes",
+    "dspark_draft_block_host",
     "dspark_verify_standard",
     "dspark_noise_words",
     "dspark_read_device_error",
@@ -74,6 +76,12 @@ def load() -> ctypes.CDLL:
             P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
             P]
         lib.dspark_draft_block_noalloc.restype = I
+        lib.dspark_draft_host_workspace_bytes.argtypes = [I, I, I, I]
+        lib.dspark_draft_host_workspace_bytes.restype = ctypes.c_size_t
+        lib.dspark_draft_block_host.argtypes = [
+            P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
+            P, P, ctypes.c_size_t, P, P]
+        lib.dspark_draft_block_host.restype = I
         lib.dspark_verify_standard.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
         lib.dspark_verify_standard.restype = I
         lib.dspark_noise_words.argtypes = [U64, U64, I, I, I, P, P, P]

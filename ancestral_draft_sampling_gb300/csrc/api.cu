@@ -147,7 +147,7 @@ cudaError_t launch_pick_plain(const DraftArgs& a, int k, int n,
 }
 
 cudaError_t proposals_adapter(const DraftArgs& a, int, int, cudaStream_t s) {
-  return launch_proposals(a, s);
+  return launch_proposals(a, 0, a.K, s);
 }
 
 // Which position kernel runs: the tensor-core kernel when the shape allows
@@ -161,9 +161,19 @@ int position_kernel_choice(const DraftArgs& a) {
   return tc_ok ? 1 : 0;
 }
 
+// Host-memory drafter logits of dspark_draft_block_host: position k's slice
+// is copied on copy_stream into a.base and signalled by ready[k]; ready[K]
+// orders the copies after the caller's earlier work on the compute stream.
+struct HostFeed {
+  const char* base_host;  // [B,K,V]
+  size_t elt;
+  cudaStream_t copy_stream;
+  cudaEvent_t* ready;     // K + 1 events
+};
+
 // The launch sequence of one draft block.
 dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
-                        StageTimer* t) {
+                        StageTimer* t, const HostFeed* feed = nullptr) {
   const int sms = sm_count() < kMaxChunks ? sm_count() : kMaxChunks;
   const int choice = position_kernel_choice(a);
   if (choice < 0) return DSPARK_ERR_UNSUPPORTED;
@@ -177,7 +187,24 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
                               (size_t)a.K * sizeof(uint32_t), a.B,
                               stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
+  if (feed) {
+    // position k's drafter logits: B rows of V values, K V apart
+    const size_t row = (size_t)a.V * feed->elt, pitch = (size_t)a.K * row;
+    if (cudaEventRecord(feed->ready[a.K], stream) != cudaSuccess ||
+        cudaStreamWaitEvent(feed->copy_stream, feed->ready[a.K], 0) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+    char* dst = static_cast<char*>(const_cast<void*>(a.base));
+    for (int k = 0; k < a.K; ++k) {
+      if (cudaMemcpy2DAsync(dst + k * row, pitch, feed->base_host + k * row,
+                            pitch, row, a.B, cudaMemcpyHostToDevice,
+                            feed->copy_stream) != cudaSuccess ||
+          cudaEventRecord(feed->ready[k], feed->copy_stream) != cudaSuccess)
+        return DSPARK_ERR_CUDA;
+    }
+  }
   for (int k = 0; k < a.K; ++k) {
+    if (feed && cudaStreamWaitEvent(stream, feed->ready[k], 0) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
     dspark_status st = timed_launch(
         t, 0, stream, tc ? launch_position_tc : launch_position_generic, a, k,
         want);
@@ -185,8 +212,38 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
     st = timed_launch(t, 1, stream, tc ? launch_pick_overlapped : launch_pick_plain,
                       a, k, n_chunks);
     if (st != DSPARK_OK) return st;
+    // with host-fed logits the GPU would idle until the next slice arrives:
+    // write this position's proposals now
+    if (feed && from_cuda(launch_proposals(a, k, 1, stream)) != DSPARK_OK)
+      return DSPARK_ERR_CUDA;
   }
+  if (feed) return DSPARK_OK;
   return timed_launch(t, 2, stream, proposals_adapter, a, 0, 0);
+}
+
+// Device workspace of dspark_draft_block_host: the draft workspace, then the
+// per-request inputs and the tokens.
+struct HostLayout {
+  size_t d0, seed, offset, greedy, pad_row, tokens, total;
+};
+
+HostLayout host_layout(int B, int K) {
+  HostLayout H;
+  size_t off = workspace_layout(B, K).total;
+  H.d0 = off;
+  off = align_up(off + (size_t)B * sizeof(int32_t), 256);
+  H.seed = off;
+  off = align_up(off + (size_t)B * sizeof(uint64_t), 256);
+  H.offset = off;
+  off = align_up(off + (size_t)B * sizeof(uint64_t), 256);
+  H.greedy = off;
+  off = align_up(off + (size_t)B, 256);
+  H.pad_row = off;
+  off = align_up(off + (size_t)B, 256);
+  H.tokens = off;
+  off = align_up(off + (size_t)B * K * sizeof(int32_t), 256);
+  H.total = off;
+  return H;
 }
 
 // ---------------------------------------------------- allocation-free scratch
@@ -319,6 +376,75 @@ dspark_status dspark_draft_block_noalloc(
   if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   return run_block(a, stream, nullptr);
+}
+
+size_t dspark_draft_host_workspace_bytes(int B, int K, int V, int r) {
+  if (!sizes_supported(B, K, V, r)) return 0;
+  return host_layout(B, K).total;
+}
+
+dspark_status dspark_draft_block_host(
+    const void* base_logits_host, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0_host,
+    const uint64_t* seed_host, const uint64_t* offset_host, float T,
+    const uint8_t* greedy_host, const uint8_t* pad_row_host, int B, int K,
+    int V, int r, void* base_dev, int32_t* tokens_host, float* logits,
+    float* draft_probs, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream, cudaStream_t copy_stream) {
+  if (!base_logits_host || !d0_host || !seed_host || !offset_host ||
+      !tokens_host || !base_dev || stream == copy_stream)
+    return DSPARK_ERR_INVALID_ARG;
+  if (B <= 0 || K <= 0 || V <= 0 || r <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (!sizes_supported(B, K, V, r)) return DSPARK_ERR_UNSUPPORTED;
+  const HostLayout H = host_layout(B, K);
+  if (!workspace || workspace_bytes < H.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return DSPARK_ERR_WORKSPACE;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* d0 = reinterpret_cast<int32_t*>(ws + H.d0);
+  uint64_t* seed = reinterpret_cast<uint64_t*>(ws + H.seed);
+  uint64_t* offset = reinterpret_cast<uint64_t*>(ws + H.offset);
+  uint8_t* greedy = greedy_host ? reinterpret_cast<uint8_t*>(ws + H.greedy) : nullptr;
+  uint8_t* pad_row = pad_row_host ? reinterpret_cast<uint8_t*>(ws + H.pad_row) : nullptr;
+  int32_t* tokens = reinterpret_cast<int32_t*>(ws + H.tokens);
+  DraftArgs a{};
+  dspark_status st = prepare_draft(
+      base_dev, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
+      pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
+      workspace_bytes, a);
+  if (st != DSPARK_OK) return st;
+  // the per-request inputs, ahead of the first position on `stream`
+  const struct { void* dst; const void* src; size_t n; } small[] = {
+      {d0, d0_host, (size_t)B * sizeof(int32_t)},
+      {seed, seed_host, (size_t)B * sizeof(uint64_t)},
+      {offset, offset_host, (size_t)B * sizeof(uint64_t)},
+      {greedy, greedy_host, (size_t)B},
+      {pad_row, pad_row_host, (size_t)B}};
+  for (const auto& c : small)
+    if (c.src && cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice,
+                                 stream) != cudaSuccess)
+      return DSPARK_ERR_CUDA;
+  cudaEvent_t ready[DSPARK_MAX_K + 1];
+  int created = 0;
+  for (; created <= K; ++created)
+    if (cudaEventCreateWithFlags(&ready[created], cudaEventDisableTiming) !=
+        cudaSuccess)
+      break;
+  if (created == K + 1) {
+    const HostFeed feed{static_cast<const char*>(base_logits_host),
+                        base_dtype == DSPARK_F32 ? (size_t)4 : (size_t)2,
+                        copy_stream, ready};
+    st = run_block(a, stream, nullptr, &feed);
+    if (st == DSPARK_OK &&
+        cudaMemcpyAsync(tokens_host, tokens, (size_t)B * K * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      st = DSPARK_ERR_CUDA;
+  } else {
+    st = DSPARK_ERR_CUDA;
+  }
+  // an event still pending is released by the runtime once it completes
+  for (int i = 0; i < created; ++i) cudaEventDestroy(ready[i]);
+  return st;
 }
 
 dspark_status dspark_verify_standard(const float* draft_probs,

@@ -248,7 +248,9 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
 // kernel waits for the previous grid before reading its statistics).
 cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
                         bool overlap_previous, cudaStream_t stream);
-cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream);
+// Proposals of positions k_first .. k_first + k_count - 1.
+cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,
+                             cudaStream_t stream);
 cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           const uint64_t* seed, const uint64_t* offset, int B,
                           int K, int V, int32_t* accepted_len,

@@ -44,13 +44,14 @@ __device__ __forceinline__ float scale(float l, float T) {
   return T == 1.0f ? l : __fdiv_rn(l, T);
 }
 
-// grid = (B*K rows, segments of a row).  q = exp(s - M) * (1 / S).  Every
-// load of a thread is issued before its first store.
+// grid = (B * k_count rows, segments of a row) for positions k_first ..
+// k_first + k_count - 1.  q = exp(s - M) * (1 / S).  Every load of a thread
+// is issued before its first store.
 template <bool kVec>
 __global__ void __launch_bounds__(kPropThreads)
-proposals_kernel(DraftArgs a) {
-  const int row = blockIdx.x;
-  const int b = row / a.K;
+proposals_kernel(DraftArgs a, int k_first, int k_count) {
+  const int b = blockIdx.x / k_count;
+  const int row = b * a.K + k_first + (int)(blockIdx.x - b * k_count);
   const int V = a.V;
   const float M = a.rowstats[2 * (size_t)row];
   const float invS = __frcp_rn(a.rowstats[2 * (size_t)row + 1]);
@@ -124,13 +125,14 @@ cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
   return cudaLaunchKernelEx(&cfg, pick_kernel, a, k, n_chunks);
 }
 
-cudaError_t launch_proposals(const DraftArgs& a, cudaStream_t stream) {
+cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,
+                             cudaStream_t stream) {
   const int seg = kPropThreads * kPropPerThread;
-  const dim3 grid(a.B * a.K, (a.V + seg - 1) / seg);
+  const dim3 grid(a.B * k_count, (a.V + seg - 1) / seg);
   if (a.V % 4 == 0)
-    proposals_kernel<true><<<grid, kPropThreads, 0, stream>>>(a);
+    proposals_kernel<true><<<grid, kPropThreads, 0, stream>>>(a, k_first, k_count);
   else
-    proposals_kernel<false><<<grid, kPropThreads, 0, stream>>>(a);
+    proposals_kernel<false><<<grid, kPropThreads, 0, stream>>>(a, k_first, k_count);
   return cudaGetLastError();
 }
 

@@ -101,7 +101,7 @@ struct TcParams {
   int stages;
   int tiles_total;
   int n_chunks;
-  uint32_t u_off, tile_off, stage_off, rows_off, bar_off;
+  uint32_t u_off, tile_off, stage_off, rows_off, rstate_off, bar_off;
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -115,16 +115,25 @@ __device__ __forceinline__ void named_sync(int id, int count) {
 }
 
 // Running state of one request in the compute warp that owns it:
-//   sum        per lane: sum of exp(s - ref) over the lane's entries;
-//   best, idx  the same in every lane: the largest decision score in this
-//              CTA so far (s + g for a sampled request, s for a greedy one)
-//              and its lowest vocab index (kNoIndex while nothing has won);
-//   ref        the same in every lane: the reference of the candidate test
-//              and the sum, max(best, posted hints) (-inf at first).
+//   sum        per lane: sum of exp(s - sref) over the lane's entries;
+//   ref, idx   the same in every lane: the reference of the candidate test,
+//              the largest decision score known (s + g for a sampled
+//              request, s for a greedy one), and its vocab index when this
+//              CTA reached it (kNoIndex when it was posted by another CTA,
+//              or nothing has won).  An entry below ref cannot be the
+//              request's winner, so this CTA's own best below ref is not
+//              kept;
+//   sref       the reference of the sum, set from the data alone (the
+//              largest scaled logit of the first tile that has one above
+//              -inf, moved only when a term would overflow), so that the sum
+//              does not depend on when hints arrive;
+//   h          exp(sref - ref), recomputed whenever ref or sref moves.
 struct RowState {
-  float sum, best, ref;
+  float sum, ref, sref, h;
   int idx;
 };
+
+
 
 // The constant of the candidate test for reference `ref`:
 // 32 + 2^-11 - ref log2(e).  While nothing has won (ref = -inf) a huge
@@ -132,6 +141,15 @@ struct RowState {
 // -inf entry adds exp2(-inf) = 0 to the sum.
 __device__ __forceinline__ float thr_const(float ref) {
   return fmaf(-fmaxf(ref, -0x1p100f), kLog2e, 32.0f + kThrSlack);
+}
+
+// exp(sref - ref): turns a sum term into the candidate test value
+// 2^(32+slack) exp(s - ref).  +inf while nothing has won (every finite entry
+// is a candidate); clamped at 2^-100 so that it never flushes to zero (and a
+// finite term times it stays finite).
+__device__ __forceinline__ float ref_factor(float sref, float ref) {
+  return ref == -INFINITY ? INFINITY
+                          : ex2_approx(fmaxf((sref - ref) * kLog2e, -100.0f));
 }
 
 // 2^(32 + slack) exp(s - best).  A sampled entry wins only if s + g > best
@@ -189,9 +207,14 @@ __device__ __forceinline__ void warp_take_best(RowState& st, float cb, int ci) {
   const uint32_t imin = __reduce_min_sync(
       0xffffffffu, key == kmax ? (uint32_t)ci : 0xffffffffu);
   const float wb = from_ordered_bits(kmax);
-  if (better(wb, (int)imin, st.best, st.idx)) {
-    st.best = wb;
+  // beats the reference, or reaches it at a lower index than a reference of
+  // this CTA's own (equal to another CTA's posted score: both are reported,
+  // the pick keeps the lower index)
+  if (wb > st.ref ||
+      (wb == st.ref && (st.idx == kNoIndex || (int)imin < st.idx))) {
+    st.ref = wb;
     st.idx = (int)imin;
+    st.h = ref_factor(st.sref, wb);
   }
 }
 
@@ -266,35 +289,59 @@ __device__ __forceinline__ void decide_sampled(RowState& st, uint32_t cand,
   warp_take_best(st, cb, ci);
 }
 
-// After a decision: a best score above the reference becomes the
-// reference; the sum is rescaled to it (while the reference is -inf the sum
-// is 0, or NaN after a NaN entry) and the four test values are recomputed.
-// Warp-uniform (best and ref are the same in every lane).
-__device__ __forceinline__ void raise_ref(RowState& st, const float (&s)[4],
-                                          float (&f)[4]) {
-  if (st.best > st.ref) {
-    if (st.ref != -INFINITY) st.sum *= ex2_approx((st.ref - st.best) * kLog2e);
-    st.ref = st.best;
-    const float tc = thr_const(st.ref);
+// The largest scaled logit of the warp's 128 entries (NaN ignored; -inf if
+// there is none above -inf).
+__device__ __forceinline__ float warp_max_scaled(const float (&s)[4]) {
+  float m = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+  for (int e = 0; e < 4; ++e)
+    if (s[e] > m) m = s[e];
+  return from_ordered_bits(__reduce_max_sync(0xffffffffu, ordered_bits(m)));
+}
+
+// The sum's terms relative to sref, scaled: f = 2^(32+slack) exp(s - sref).
+// While sref is unset (-inf) every term above -inf is +inf, which makes it a
+// candidate; the candidate path then sets sref (rebase_sum).
+__device__ __forceinline__ void sum_terms(const RowState& st,
+                                          const float (&s)[4], float (&f)[4]) {
+  const float tc = thr_const(st.sref);
+#pragma unroll
+  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
+}
+
+// A term at or above 2^100 (always a candidate) means sref is unset or s -
+// sref nears float32's range: sref moves to this tile's largest scaled
+// logit (a value fixed by the data), the sum is rescaled to it (from an
+// unset sref the sum is 0, or NaN after a NaN entry) and the terms are
+// recomputed.  Warp-uniform.
+__device__ __forceinline__ void rebase_sum(RowState& st, const float (&s)[4],
+                                           float (&f)[4]) {
+  const bool big = f[0] >= 0x1p100f || f[1] >= 0x1p100f ||
+                   f[2] >= 0x1p100f || f[3] >= 0x1p100f;
+  if (__any_sync(0xffffffffu, big)) {
+    const float r = warp_max_scaled(s);
+    if (r > st.sref) {
+      st.sum *= ex2_approx((st.sref - r) * kLog2e);
+      st.sref = r;
+      st.h = ref_factor(r, st.ref);
+      sum_terms(st, s, f);
+    }
   }
 }
 
-// The sum-exp of four entries relative to the reference: the test values
-// f = 2^(32+slack) exp(s - ref), scaled back.
+// The sum-exp of four entries relative to sref: the terms, scaled back.
 __device__ __forceinline__ void accumulate(RowState& st, const float (&f)[4]) {
   st.sum = fmaf(__fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])),
                 kSumScale, st.sum);
 }
 
 // A best score posted by another CTA (order-preserving bits, 0 = none)
-// raises the reference of the candidate test and of the sum.
+// raises the reference of the candidate test.
 __device__ __forceinline__ void adopt_hint(RowState& st, uint32_t h) {
   if (h > ordered_bits(st.ref)) {
-    const float r = from_ordered_bits(h);
-    if (st.ref != -INFINITY) st.sum *= ex2_approx((st.ref - r) * kLog2e);
-    st.ref = r;
+    st.ref = from_ordered_bits(h);
+    st.idx = kNoIndex;  // another CTA's entry
+    st.h = ref_factor(st.sref, st.ref);
   }
 }
 
@@ -304,17 +351,16 @@ __device__ __forceinline__ void sampled_step(const RowConst& rc,
                                              const float (&s)[4], int v,
                                              RowState& st) {
   const uint4 w = row_noise(rc, v);
-  const float tc = thr_const(st.ref);
   float f[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
-  const uint32_t cand = (__uint2float_rz(w.x) < f[0] ? 1u : 0u) |
-                        (__uint2float_rz(w.y) < f[1] ? 2u : 0u) |
-                        (__uint2float_rz(w.z) < f[2] ? 4u : 0u) |
-                        (__uint2float_rz(w.w) < f[3] ? 8u : 0u);
+  sum_terms(st, s, f);
+  const float h = st.h;
+  const uint32_t cand = (__uint2float_rz(w.x) < __fmul_ru(f[0], h) ? 1u : 0u) |
+                        (__uint2float_rz(w.y) < __fmul_ru(f[1], h) ? 2u : 0u) |
+                        (__uint2float_rz(w.z) < __fmul_ru(f[2], h) ? 4u : 0u) |
+                        (__uint2float_rz(w.w) < __fmul_ru(f[3], h) ? 8u : 0u);
   if (__any_sync(0xffffffffu, cand != 0u)) {
     decide_sampled(st, cand, s, w, v);
-    raise_ref(st, s, f);
+    rebase_sum(st, s, f);
   }
   accumulate(st, f);
 }
@@ -346,29 +392,23 @@ __device__ __forceinline__ void sampled_first(const RowConst& rc,
     }
   }
   decide_sampled(st, first, s, w, v);
-  if (st.best > st.ref) {  // the reference is -inf here: the sum is 0 or NaN
-    st.ref = st.best;
-  }
-  const float tc = thr_const(st.ref);
   float f[4];
+  sum_terms(st, s, f);
+  rebase_sum(st, s, f);  // sets sref on the first tile with a value
+  const float h = st.h;
   uint32_t cand = 0;
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    f[e] = test_value(s[e], tc);
-    cand |= (__uint2float_rz(word_of(w, e)) < f[e] ? 1u : 0u) << e;
-  }
+  for (int e = 0; e < 4; ++e)
+    cand |= (__uint2float_rz(word_of(w, e)) < __fmul_ru(f[e], h) ? 1u : 0u) << e;
   cand &= ~first;
-  if (__any_sync(0xffffffffu, cand != 0u)) {
-    decide_sampled(st, cand, s, w, v);
-    raise_ref(st, s, f);
-  }
+  if (__any_sync(0xffffffffu, cand != 0u)) decide_sampled(st, cand, s, w, v);
   accumulate(st, f);
 }
 
 // A greedy request: no noise; an entry is a candidate iff s > best.
 __device__ __forceinline__ void greedy_step(const float (&s)[4], int v,
                                             RowState& st) {
-  const float old_best = st.best;
+  const float old_best = st.ref;
   uint32_t cand = (s[0] > old_best ? 1u : 0u) | (s[1] > old_best ? 2u : 0u) |
                   (s[2] > old_best ? 4u : 0u) | (s[3] > old_best ? 8u : 0u);
   if (__any_sync(0xffffffffu, cand != 0u)) {
@@ -385,10 +425,8 @@ __device__ __forceinline__ void greedy_step(const float (&s)[4], int v,
     warp_take_best(st, cb, ci);
   }
   float f[4];
-  const float tc = thr_const(st.ref);
-#pragma unroll
-  for (int e = 0; e < 4; ++e) f[e] = test_value(s[e], tc);
-  raise_ref(st, s, f);
+  sum_terms(st, s, f);
+  rebase_sum(st, s, f);
   accumulate(st, f);
 }
 
@@ -660,14 +698,18 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int c = 0; c < nvalid; ++c)
       padmask |= ((rows[col0 + c].flags & kRowPad) ? 1u : 0u) << c;
     const float T = a.T;
-    RowState st[kMaxRows];
+    // The warp-uniform part of each request's state (best, ref, sref, idx)
+    // lives in shared memory between row steps, the per-lane sums in
+    // registers.  Every lane stores the same values and reads back its own
+    // store, so only the initialisation (by lanes 0..3) needs a warp sync.
+    float sums[kMaxRows];
+    float4* rstate = reinterpret_cast<float4*>(smem + P.rstate_off) + cw * kMaxRows;
 #pragma unroll
-    for (int i = 0; i < kMaxRows; ++i) {
-      st[i].sum = 0.0f;
-      st[i].best = -INFINITY;  // nothing to beat yet
-      st[i].ref = -INFINITY;
-      st[i].idx = kNoIndex;
-    }
+    for (int i = 0; i < kMaxRows; ++i) sums[i] = 0.0f;
+    if (lane < kMaxRows)  // nothing won, no reference yet
+      rstate[lane] = make_float4(-INFINITY, -INFINITY, INFINITY,
+                                 __int_as_float(kNoIndex));
+    __syncwarp();
 
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
@@ -737,23 +779,29 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           scaled4<kUnitT>(l4, T, sv);
           const RowConst& rc = rows[b];
           const uint32_t h = __shfl_sync(0xffffffffu, hint_in, i);
+          const float4 q = rstate[i];
+          RowState st{sums[i], q.x, q.y, q.z, __float_as_int(q.w)};  // ref, sref, h, idx
           if ((greedy_mask >> i) & 1u) {
-            greedy_step(sv, v, st[i]);
+            greedy_step(sv, v, st);
           } else {
-            adopt_hint(st[i], h);
+            adopt_hint(st, h);
             // first tile: bootstrap the reference; afterwards the steady
             // state (which also handles a reference still at -inf)
-            if (t == 0 && st[i].ref == -INFINITY)
-              sampled_first(rc, sv, v, st[i]);
+            if (t == 0 && st.ref == -INFINITY)
+              sampled_first(rc, sv, v, st);
             else
-              sampled_step(rc, sv, v, st[i]);
+              sampled_step(rc, sv, v, st);
           }
+          sums[i] = st.sum;
+          rstate[i] = make_float4(st.ref, st.sref, st.h, __int_as_float(st.idx));
         }
         // post bests that beat the hint read for this tile
+        __syncwarp();
         uint32_t mine = 0;
-#pragma unroll
-        for (int i = 0; i < kMaxRows; ++i)
-          if (lane == i && st[i].idx != kNoIndex) mine = ordered_bits(st[i].best);
+        if (lane < kMaxRows) {
+          const float4 q = rstate[lane];
+          if (__float_as_int(q.w) != kNoIndex) mine = ordered_bits(q.x);
+        }
         if (hint_ptr && mine > hint_in) atomicMax(hint_ptr, mine);
       }
       if (storer) bulk_wait_read_all();  // the store has read the tile
@@ -766,15 +814,16 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int i = 0; i < kMaxRows; ++i) {
       const int b = cw + kComputeWarps * i;
       if (b >= a.B) break;
-      float sum = st[i].sum;
+      float sum = sums[i];
+      const float4 q = rstate[i];
 #pragma unroll
       for (int mask = 16; mask > 0; mask >>= 1)
         sum = __fadd_rn(sum, __shfl_xor_sync(0xffffffffu, sum, mask));
       if (lane == 0) {
         ChunkStat cs;
-        cs.best = st[i].best;
-        cs.idx = st[i].idx;
-        cs.m = st[i].ref;  // the reference of the sum (-inf: nothing won)
+        cs.idx = __float_as_int(q.w);
+        cs.best = cs.idx == kNoIndex ? -INFINITY : q.x;  // this CTA's own winner
+        cs.m = q.y;  // the reference of the sum (-inf: none set)
         cs.s = sum;
         a.stats[(size_t)b * kMaxChunks + chunk] = cs;
       }
@@ -807,7 +856,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 struct Layout {
   int bpad, stages;
-  uint32_t u_off, tile_off, stage_off, rows_off, bar_off;
+  uint32_t u_off, tile_off, stage_off, rows_off, rstate_off, bar_off;
   size_t smem;
 };
 
@@ -820,15 +869,17 @@ Layout make_layout(int B, int r, int base_elt) {
   const size_t tiles = 2 * (size_t)L.bpad * kTileV * 4;
   const size_t stage = base_elt == 2 ? (size_t)L.bpad * kTileV * 2 : 0;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowConst), 16);
+  const size_t rstate = (size_t)kComputeWarps * kMaxRows * 16;
   const size_t bars = (2 * kMaxStages + 11) * 8 + 16;
-  const size_t fixed = u + tiles + stage + rows + bars + 1024;
+  const size_t fixed = u + tiles + stage + rows + rstate + bars + 1024;
   L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
   if (L.stages > kMaxStages) L.stages = kMaxStages;
   L.u_off = (uint32_t)((size_t)L.stages * kStageBytes);
   L.tile_off = (uint32_t)(L.u_off + u);
   L.stage_off = (uint32_t)(L.tile_off + tiles);
   L.rows_off = (uint32_t)(L.stage_off + stage);
-  L.bar_off = (uint32_t)(L.rows_off + rows);
+  L.rstate_off = (uint32_t)(L.rows_off + rows);
+  L.bar_off = (uint32_t)(L.rstate_off + rstate);
   L.smem = L.bar_off + bars + 1024;
   return L;
 }
@@ -929,6 +980,7 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
   P.tile_off = L.tile_off;
   P.stage_off = L.stage_off;
   P.rows_off = L.rows_off;
+  P.rstate_off = L.rstate_off;
   P.bar_off = L.bar_off;
   const bool unit = a.T == 1.0f;
   const bool pdl = k > 0;

@@ -177,6 +177,51 @@ DSPARK_API dspark_status dspark_draft_block_noalloc(
     int32_t* tokens, float* logits, float* draft_probs, cudaStream_t stream);
 
 /*
+ * dspark_draft_host_workspace_bytes -- device workspace of
+ * dspark_draft_block_host: that of dspark_draft_block plus room for the
+ * per-request inputs and the tokens (0 if the sizes are unsupported).
+ */
+DSPARK_API size_t dspark_draft_host_workspace_bytes(int B, int K, int V, int r);
+
+/*
+ * dspark_draft_block_host -- dspark_draft_block with its inputs in host
+ * memory and the drafted tokens returned to host memory; the call issues
+ * the copies itself.
+ *
+ *   base_logits_host [B,K,V] base_dtype in host memory.  Page-locked memory
+ *                lets the copies run asynchronously (with pageable memory
+ *                each copy synchronises).
+ *   d0_host, seed_host, offset_host [B]; greedy_host, pad_row_host [B] or
+ *                NULL: host memory, meanings as in dspark_draft_block.
+ *   U, Wb        device, as in dspark_draft_block (resident weights).
+ *   base_dev     device [B,K,V] base_dtype buffer that receives the drafter
+ *                logits (16-byte aligned; read by this call's kernels).
+ *   tokens_host  [B,K] int32 host out, copied on `stream` after the block.
+ *   logits, draft_probs  device [B,K,V] float32 outputs.
+ *   workspace    device, dspark_draft_host_workspace_bytes(B,K,V,r) bytes,
+ *                256-byte aligned.
+ *   stream       the compute stream; copy_stream a second stream for the
+ *                drafter-logit copies (must differ from stream).
+ * Position k's drafter logits (B rows of V values, one 2-D copy) travel on
+ * copy_stream while earlier positions compute on stream.  Position k waits
+ * for its own copy only, and its proposals are written right after its pick,
+ * so the block's work hides behind the copies.  The copies start after all
+ * work issued to `stream` before the call.  Outputs are identical to
+ * dspark_draft_block's.  Host buffers must stay valid until `stream` has
+ * passed the end of the call.  The call creates and destroys K+1 CUDA
+ * events.  It may be captured in a CUDA graph: its event waits join
+ * copy_stream to the capture of `stream`.
+ */
+DSPARK_API dspark_status dspark_draft_block_host(
+    const void* base_logits_host, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0_host,
+    const uint64_t* seed_host, const uint64_t* offset_host, float T,
+    const uint8_t* greedy_host, const uint8_t* pad_row_host, int B, int K,
+    int V, int r, void* base_dev, int32_t* tokens_host, float* logits,
+    float* draft_probs, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream, cudaStream_t copy_stream);
+
+/*
  * dspark_verify_standard -- standard token-level rejection sampling of the
  * drafts (PR #21, "2. Golden sampling semantics": the default rule), for B
  * requests.

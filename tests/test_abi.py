@@ -143,3 +143,41 @@ def test_read_device_error_rejects_null(lib):
     code = ctypes.c_int(0)
     assert lib.dspark_read_device_error(None, ctypes.byref(code), None) == INVALID
     assert lib.dspark_read_device_error(FAKE, None, None) == INVALID
+
+
+def test_host_workspace_bytes(lib):
+    wh = lib.dspark_draft_host_workspace_bytes
+    ws = lib.dspark_draft_workspace_bytes
+    assert wh(88, 7, 200064, 256) > ws(88, 7, 200064, 256)
+    assert wh(88, 7, 200064, 256) % 256 == 0
+    assert wh(0, 7, 100, 64) == 0
+
+
+def _host_args(lib, **over):
+    import ctypes
+    B, K, V, r = 4, 3, 1024, 64
+    host = (ctypes.c_uint8 * 64)()  # host stand-in, never read: every call fails first
+    h = ctypes.addressof(host)
+    a = dict(base=h, base_dtype=0, U=FAKE, Wb=FAKE, w_dtype=1, d0=h, seed=h,
+             offset=h, T=1.0, greedy=None, pad_row=None, B=B, K=K, V=V, r=r,
+             base_dev=FAKE, tokens=h, logits=FAKE, probs=FAKE, ws=FAKE,
+             ws_bytes=lib.dspark_draft_host_workspace_bytes(B, K, V, r),
+             stream=None, copy_stream=1)
+    a.update(over)
+    return host, a
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(base=None), 1), (dict(d0=None), 1), (dict(tokens=None), 1),
+    (dict(base_dev=None), 1), (dict(copy_stream=None), 1),   # same as stream
+    (dict(T=0.0), 1), (dict(base_dev=FAKE + 8), 1), (dict(r=72), 2),
+    (dict(ws=None), 3), (dict(ws_bytes=256), 3), (dict(ws=FAKE + 16), 3),
+])
+def test_draft_block_host_rejects_bad_arguments(lib, over, want):
+    host, a = _host_args(lib, **over)
+    st = lib.dspark_draft_block_host(
+        a["base"], a["base_dtype"], a["U"], a["Wb"], a["w_dtype"], a["d0"],
+        a["seed"], a["offset"], a["T"], a["greedy"], a["pad_row"], a["B"],
+        a["K"], a["V"], a["r"], a["base_dev"], a["tokens"], a["logits"],
+        a["probs"], a["ws"], a["ws_bytes"], a["stream"], a["copy_stream"])
+    assert st == want
