@@ -58,16 +58,15 @@ constexpr int kTileV = 128;                        // vocab rows per tile (M)
 constexpr int kKChunk = 64;                        // r per pipeline stage
 constexpr int kBoxBytes = 64 * kKChunk * 2;        // one 64x64 bf16 box
 constexpr int kStageBytes = 2 * kBoxBytes;         // 128 vocab x 64 r
-constexpr int kComputeWarps = 24;
-constexpr int kThreads = 32 * (2 + kComputeWarps);
+constexpr int kDrainWarps = 8;                     // two per TMEM lane quarter
+constexpr int kComputeWarps = 22;                  // the decision warps
+constexpr int kWorkWarps = kDrainWarps + kComputeWarps;
+constexpr int kThreads = 32 * (2 + kWorkWarps);
+constexpr int kWorkThreads = 32 * kWorkWarps;      // set-up and u gather
+constexpr int kDrainThreads = 32 * kDrainWarps;
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kMaxBpad = 96;
-constexpr int kColGroups = kComputeWarps / 4;
-constexpr int kMaxGcols = (kMaxBpad / kColGroups + 3) / 4 * 4;
-constexpr int kMaxRows = kMaxGcols / 4;
-__host__ __device__ constexpr int group_cols(int bpad) {
-  return ((bpad + kColGroups - 1) / kColGroups + 3) / 4 * 4;
-}
+constexpr int kMaxRows = (kMaxBpad + kComputeWarps - 1) / kComputeWarps;  // requests per compute warp
 constexpr uint32_t kTmemCols = 256;                // two accumulators
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSpin = 1u << 22;
@@ -170,19 +169,6 @@ __device__ __forceinline__ float pick4(const float (&a)[4], int e) {
 template <bool kUnitT>
 __device__ __forceinline__ float scale(float l, float T) {
   return kUnitT ? l : __fdiv_rn(l, T);
-}
-
-// tcgen05.ld of four consecutive columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-  uint32_t r0, r1, r2, r3;
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(taddr)
-               : "memory");
-  v[0] = __uint_as_float(r0);
-  v[1] = __uint_as_float(r1);
-  v[2] = __uint_as_float(r2);
-  v[3] = __uint_as_float(r3);
 }
 
 // Float32 -> uint32 map that preserves order (for finite and infinite
@@ -464,7 +450,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   uint64_t* stage_free = tile_free + 2;
   uint64_t* mma_done = stage_free + 1;
   uint64_t* u_ready = mma_done + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(u_ready + 1);
+  uint64_t* drained = u_ready + 1;  // [2]: the drain warps have filled a buffer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const DraftArgs& a = P.a;
@@ -489,13 +476,14 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], kComputeThreads);
+      mbar_init(&acc_empty[i], kDrainThreads);
       mbar_init(&base_full[i], 1);
-      mbar_init(&tile_free[i], kComputeThreads);
+      mbar_init(&tile_free[i], kComputeThreads + 1);  // + the storer
+      mbar_init(&drained[i], kDrainThreads);
     }
-    mbar_init(stage_free, kComputeThreads);
+    mbar_init(stage_free, kDrainThreads);
     mbar_init(mma_done, 1);
-    mbar_init(u_ready, kComputeThreads);
+    mbar_init(u_ready, kWorkThreads);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -512,7 +500,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     // per-request constants (inputs only: they may be read before the
     // previous position's kernel has finished)
     const int ct = threadIdx.x - 64;
-    for (int b = ct; b < P.bpad; b += kComputeThreads) {
+    for (int b = ct; b < P.bpad; b += kWorkThreads) {
       RowConst rc;
       uint32_t k0 = 0, k1 = 0, c2 = 0, c3 = 0;
       rc.flags = 0;
@@ -654,7 +642,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     const int ct = threadIdx.x - 64;
     const int pieces = a.r / 8;
     const uint16_t* U = static_cast<const uint16_t*>(a.U);
-    for (int i = ct; i < P.bpad * pieces; i += kComputeThreads) {
+    for (int i = ct; i < P.bpad * pieces; i += kWorkThreads) {
       const int b = i / pieces, piece = i - b * pieces;
       const int c = piece >> 3, p = piece & 7;
       uint4 val = make_uint4(0u, 0u, 0u, 0u);
@@ -672,12 +660,92 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     }
     fence_proxy_async_smem();  // the MMA reads u through the async proxy
     mbar_arrive(u_ready);
-    const int cw = warp - 2;
-    const int q = warp & 3;                  // TMEM lane quarter
-    const int gcols = group_cols(P.bpad);
-    const int col0 = (cw >> 2) * gcols;
-    const int m = 32 * q + lane;             // drained vocab row of the tile
-    const bool storer = cw == 0 && lane == 0;
+    if (warp < 2 + kDrainWarps) {
+      // ----------------------------------------------------------- drain
+      // Warp q drains TMEM lanes 32q.. (vocab rows m of the tile) for every
+      // request, adds the bias into the drafter-logit tile in place (l =
+      // bias on padding rows), and then the tile is stored with one TMA
+      // store while the compute warps take the previous tile.
+      const int q = warp & 3;                // TMEM lane quarter
+      const int h = (warp - 2) >> 2;         // column half: 16-column groups 2g+h
+      const int m = 32 * q + lane;           // drained vocab row of the tile
+      const bool storer = warp == 2 && lane == 0;
+      // bit c & 31 of word c >> 5: request c is a padding row
+      uint32_t pad0 = 0, pad1 = 0, pad2 = 0;
+      static_assert(kMaxBpad <= 96, "three padding words");
+      for (int c = 0; c < a.B; ++c)
+        if (rows[c].flags & kRowPad) {
+          const uint32_t bit = 1u << (c & 31);
+          if (c < 32) pad0 |= bit; else if (c < 64) pad1 |= bit; else pad2 |= bit;
+        }
+      for (int t = 0; t < n_tiles; ++t) {
+        const int buf = t & 1;
+        const uint32_t ph = (uint32_t)(t >> 1) & 1u;
+        const int v0 = (t_begin + t) * kTileV;
+        float* tile = tiles + (size_t)buf * tile_floats;
+        // bf16 logits arrive in the staging tile, so the f32 buffer is
+        // written here: it must be released (tile t-2 read by the compute
+        // warps and the store) first; f32 logits were loaded into it by TMA
+        // only after that release
+        bool ok = !*abort_flag &&
+                  (!kStaged || mbar_wait(&tile_free[buf], ph ^ 1u, kSpin)) &&
+                  mbar_wait(kStaged ? &base_full[0] : &base_full[buf],
+                            kStaged ? ((uint32_t)t & 1u) : ph, kSpin) &&
+                  mbar_wait(&acc_full[buf], ph, kSpin);
+        ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
+        if (ok) {
+          tc_fence_after();
+          const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
+                                 (uint32_t)buf * kAccCols;
+          float* col = tile + m;
+#pragma unroll 1
+          for (int c0 = 16 * h; c0 < a.B; c0 += 32) {
+            float bias[16];
+            tmem_ld16(taddr + (uint32_t)c0, bias);  // within the 128 columns
+            tmem_ld_wait();
+            const uint32_t pw =
+                (c0 < 32 ? pad0 : (c0 < 64 ? pad1 : pad2)) >> (c0 & 31);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int c = c0 + j;
+              if (c >= a.B) break;
+              float x;
+              if (kStaged)
+                x = __uint_as_float(
+                    (uint32_t)reinterpret_cast<const uint16_t*>(stage)[c * kTileV + m] << 16);
+              else
+                x = col[c * kTileV];
+              col[c * kTileV] = ((pw >> j) & 1u) ? bias[j] : __fadd_rn(x, bias[j]);
+            }
+          }
+          // the ragged last tile: vocab rows past V become -inf, which no
+          // decision admits and the sum ignores (the logits store clips them)
+          if (v0 + kTileV > a.V && v0 + m >= a.V) {
+            for (int c = 0; c < a.B; ++c)
+              if (((c >> 4) & 1) == h) col[c * kTileV] = -INFINITY;
+          }
+          tc_fence_before();
+        } else if (!*abort_flag) {
+          fail(kDevErrTimeout);
+        }
+        mbar_arrive(&acc_empty[buf]);
+        if (kStaged) mbar_arrive(stage_free);
+        fence_proxy_async_smem();         // the tile store reads these writes
+        named_sync(1, kDrainThreads);     // the whole tile is drained
+        if (storer && !*abort_flag) {
+          tma_store_2d(&out_map, tile, v0, 0);
+          bulk_commit();
+        }
+        mbar_arrive(&drained[buf]);
+        if (storer) {
+          bulk_wait_read_all();  // the store has read the tile
+          mbar_arrive(&tile_free[buf]);
+        }
+      }
+      if (storer) bulk_wait_all();
+    } else {
+    // ------------------------------------------------------------- compute
+    const int cw = warp - 2 - kDrainWarps;
     // lane i < kMaxRows: the best-score hint of this warp's row i (sampled
     // requests only)
     uint32_t* hint_ptr = nullptr;
@@ -686,22 +754,18 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       if (lane < kMaxRows && hb < a.B && !(rows[hb].flags & kRowGreedy))
         hint_ptr = a.hints + (size_t)hb * kHintRowWords + P.k;
     }
-    // drained columns that hold requests (< B), and which are padding rows
-    const int nvalid = a.B - col0 < 0 ? 0 : (a.B - col0 < gcols ? a.B - col0 : gcols);
     uint32_t greedy_mask = 0;  // bit i: this warp's row i is greedy
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
       const int b = cw + kComputeWarps * i;
       if (b < a.B && (rows[b].flags & kRowGreedy)) greedy_mask |= 1u << i;
     }
-    uint32_t padmask = 0;
-    for (int c = 0; c < nvalid; ++c)
-      padmask |= ((rows[col0 + c].flags & kRowPad) ? 1u : 0u) << c;
     const float T = a.T;
-    // The warp-uniform part of each request's state (best, ref, sref, idx)
+    // The warp-uniform part of each request's state (ref, sref, h, idx)
     // lives in shared memory between row steps, the per-lane sums in
     // registers.  Every lane stores the same values and reads back its own
-    // store, so only the initialisation (by lanes 0..3) needs a warp sync.
+    // store, so only the initialisation (by lanes 0..kMaxRows-1) needs a
+    // warp sync.
     float sums[kMaxRows];
     float4* rstate = reinterpret_cast<float4*>(smem + P.rstate_off) + cw * kMaxRows;
 #pragma unroll
@@ -715,60 +779,12 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       const int buf = t & 1;
       const uint32_t ph = (uint32_t)(t >> 1) & 1u;
       const int v0 = (t_begin + t) * kTileV;
-      float* tile = tiles + (size_t)buf * tile_floats;
+      const float* tile = tiles + (size_t)buf * tile_floats;
       const uint32_t hint_in = hint_ptr ? __ldcg(hint_ptr) : 0u;
-      // drain: l = base + bias for this warp's (vocab row m, request) block
-      bool ok = !*abort_flag &&
-                mbar_wait(kStaged ? &base_full[0] : &base_full[buf],
-                          kStaged ? ((uint32_t)t & 1u) : ph, kSpin) &&
-                mbar_wait(&acc_full[buf], ph, kSpin);
-      ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
-      if (ok) {
-        tc_fence_after();
-        const uint32_t taddr = tmem_base + ((uint32_t)(32 * q) << 16) +
-                               (uint32_t)buf * kAccCols + (uint32_t)col0;
-        float bias[kMaxGcols];
-#pragma unroll
-        for (int c = 0; c < kMaxGcols; c += 4)
-          if (c < gcols) {
-            float q4[4];
-            tmem_ld4(taddr + (uint32_t)c, q4);
-            bias[c] = q4[0];
-            bias[c + 1] = q4[1];
-            bias[c + 2] = q4[2];
-            bias[c + 3] = q4[3];
-          }
-        tmem_ld_wait();
-        float* col = tile + col0 * kTileV + m;
-#pragma unroll
-        for (int c = 0; c < kMaxGcols; ++c) {
-          if (c >= nvalid) break;
-          float x;
-          if (kStaged)
-            x = __uint_as_float(
-                (uint32_t)reinterpret_cast<const uint16_t*>(stage)[(col0 + c) * kTileV + m] << 16);
-          else
-            x = col[c * kTileV];
-          col[c * kTileV] = ((padmask >> c) & 1u) ? bias[c] : __fadd_rn(x, bias[c]);
-        }
-        // the ragged last tile: vocab rows past V become -inf, which no
-        // decision admits and the sum ignores (the logits store clips them)
-        if (v0 + kTileV > a.V && v0 + m >= a.V) {
-          for (int c = 0; c < nvalid; ++c) col[c * kTileV] = -INFINITY;
-        }
-        tc_fence_before();
-      } else if (!*abort_flag) {
-        fail(kDevErrTimeout);
-      }
-      mbar_arrive(&acc_empty[buf]);
-      if (kStaged) mbar_arrive(stage_free);
-      fence_proxy_async_smem();  // the tile store reads these writes
-      named_sync(1, kComputeThreads);  // the tile holds the biased logits
-      if (storer && !*abort_flag) {
-        tma_store_2d(&out_map, tile, v0, 0);
-        bulk_commit();
-      }
-      if (!*abort_flag) {
+      // the drain warps have written this tile's biased logits
+      const bool ok = !*abort_flag && mbar_wait(&drained[buf], ph, kSpin);
+      if (!ok && !*abort_flag) fail(kDevErrTimeout);
+      if (ok && !*abort_flag) {
         const int v = v0 + 4 * lane;
 #pragma unroll
         for (int i = 0; i < kMaxRows; ++i) {
@@ -804,10 +820,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         }
         if (hint_ptr && mine > hint_in) atomicMax(hint_ptr, mine);
       }
-      if (storer) bulk_wait_read_all();  // the store has read the tile
       mbar_arrive(&tile_free[buf]);
     }
-    if (storer) bulk_wait_all();
     // chunk statistics: best score and index (already warp-wide), the
     // lanes' sums (same reference) added by a butterfly
 #pragma unroll
@@ -827,6 +841,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         cs.s = sum;
         a.stats[(size_t)b * kMaxChunks + chunk] = cs;
       }
+    }
     }
   }
 
@@ -870,7 +885,7 @@ Layout make_layout(int B, int r, int base_elt) {
   const size_t stage = base_elt == 2 ? (size_t)L.bpad * kTileV * 2 : 0;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowConst), 16);
   const size_t rstate = (size_t)kComputeWarps * kMaxRows * 16;
-  const size_t bars = (2 * kMaxStages + 11) * 8 + 16;
+  const size_t bars = (2 * kMaxStages + 13) * 8 + 16;
   const size_t fixed = u + tiles + stage + rows + rstate + bars + 1024;
   L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
   if (L.stages > kMaxStages) L.stages = kMaxStages;
