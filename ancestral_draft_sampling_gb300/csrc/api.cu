@@ -101,7 +101,7 @@ dspark_status prepare_draft(
   char* ws = static_cast<char*>(workspace);
   a.stats = reinterpret_cast<ChunkStat*>(ws + L.stats);
   a.rowstats = reinterpret_cast<float*>(ws + L.rowstats);
-  a.hints = reinterpret_cast<uint32_t*>(ws + L.hints);
+  a.hints = reinterpret_cast<unsigned long long*>(ws + L.hints);
   a.control = reinterpret_cast<int*>(ws + L.control);
 
   return DSPARK_OK;
@@ -133,17 +133,18 @@ dspark_status timed_launch(StageTimer* t, int cls, cudaStream_t stream,
   return DSPARK_OK;
 }
 
-// The pick after a tensor-core position overlaps that kernel's end (both
-// are launched for programmatic dependent launch); after the FFMA kernel it
-// is an ordinary launch.
-cudaError_t launch_pick_overlapped(const DraftArgs& a, int k, int n,
-                                   cudaStream_t s) {
-  return launch_pick(a, k, n, true, s);
+// The pick of the last tensor-core position overlaps that kernel's end (both
+// are launched for programmatic dependent launch) and takes d_{K-1} from the
+// decision keys; after each FFMA position the pick is an ordinary launch
+// and merges the winner from the statistics.
+cudaError_t launch_pick_keys(const DraftArgs& a, int k, int n,
+                             cudaStream_t s) {
+  return launch_pick(a, k, n, k & 1, true, true, s);
 }
 
 cudaError_t launch_pick_plain(const DraftArgs& a, int k, int n,
                               cudaStream_t s) {
-  return launch_pick(a, k, n, false, s);
+  return launch_pick(a, k, n, 0, false, false, s);
 }
 
 cudaError_t proposals_adapter(const DraftArgs& a, int, int, cudaStream_t s) {
@@ -178,13 +179,13 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   const int choice = position_kernel_choice(a);
   if (choice < 0) return DSPARK_ERR_UNSUPPORTED;
   const bool tc = choice == 1;
-  // position kernels fill n_slots statistics slots per request; the pick
-  // merges them in slot order
+  // position kernels fill n_chunks statistics slots per request; they are
+  // merged in slot order
   const int want = tc ? position_tc_chunks(a.V, sms) : sms;
   const int n_chunks = tc ? want : generic_chunks_used(a.V, want);
-  // the cross-CTA best-score hints of every position start at zero
-  if (tc && cudaMemset2DAsync(a.hints, kHintRowWords * sizeof(uint32_t), 0,
-                              (size_t)a.K * sizeof(uint32_t), a.B,
+  // the decision keys of every position start at zero (no winner)
+  if (tc && cudaMemset2DAsync(a.hints, kHintRowKeys * sizeof(uint64_t), 0,
+                              (size_t)a.K * sizeof(uint64_t), a.B,
                               stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (feed) {
@@ -202,6 +203,10 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
         return DSPARK_ERR_CUDA;
     }
   }
+  // Tensor-core positions follow one another directly: position k reads
+  // d_{k-1} from the decision keys and merges position k-1's statistics
+  // itself; one pick after the last position finishes the block.  Each
+  // FFMA position is followed by its pick.
   for (int k = 0; k < a.K; ++k) {
     if (feed && cudaStreamWaitEvent(stream, feed->ready[k], 0) != cudaSuccess)
       return DSPARK_ERR_CUDA;
@@ -209,13 +214,24 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
         t, 0, stream, tc ? launch_position_tc : launch_position_generic, a, k,
         want);
     if (st != DSPARK_OK) return st;
-    st = timed_launch(t, 1, stream, tc ? launch_pick_overlapped : launch_pick_plain,
-                      a, k, n_chunks);
-    if (st != DSPARK_OK) return st;
+    if (!tc || k == a.K - 1) {
+      st = timed_launch(t, 1, stream, tc ? launch_pick_keys : launch_pick_plain,
+                        a, k, n_chunks);
+      if (st != DSPARK_OK) return st;
+    }
     // with host-fed logits the GPU would idle until the next slice arrives:
-    // write this position's proposals now
-    if (feed && from_cuda(launch_proposals(a, k, 1, stream)) != DSPARK_OK)
-      return DSPARK_ERR_CUDA;
+    // write each position's proposals as soon as its (M, S) exist (after
+    // its pick, or after the next tensor-core position has merged them)
+    if (feed) {
+      int lo = k, hi = k;  // FFMA: position k's pick has just run
+      if (tc) {            // position k merged k-1; the last pick ran for K-1
+        lo = k - 1 < 0 ? 0 : k - 1;
+        hi = k == a.K - 1 ? k : k - 1;
+      }
+      if (hi >= lo &&
+          from_cuda(launch_proposals(a, lo, hi - lo + 1, stream)) != DSPARK_OK)
+        return DSPARK_ERR_CUDA;
+    }
   }
   if (feed) return DSPARK_OK;
   return timed_launch(t, 2, stream, proposals_adapter, a, 0, 0);

@@ -18,7 +18,7 @@
 namespace dspark {
 
 // ---------------------------------------------------------------- limits
-constexpr int kMaxChunks = 1024;       // vocab chunks per position (grid.x)
+constexpr int kMaxChunks = 512;        // vocab chunks per position (grid.x)
 constexpr int kNoIndex = 0x7fffffff;   // "no non-NaN candidate yet"
 constexpr int kNoiseDraft = 0;         // counter stream ids
 constexpr int kNoiseAccept = 1;
@@ -167,24 +167,79 @@ __device__ __forceinline__ ChunkStat empty_stat() {
   return e;
 }
 
+// Float32 -> uint32 map that preserves order (for finite and infinite
+// values): flip every bit of negatives, set the sign bit of the others.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float from_ordered_bits(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// Decision key of a winner (score, index): the score's order-preserving
+// bits above the complement of the index, so the unsigned maximum of keys
+// is the candidate order of better() (larger score, then lower index).  A
+// winner's score is never NaN and its key never 0; 0 means "no winner".
+__device__ __forceinline__ unsigned long long decision_key(float score,
+                                                           int idx) {
+  return ((unsigned long long)ordered_bits(score) << 32) |
+         (unsigned long long)(0xffffffffu - (uint32_t)idx);
+}
+
+// The token a key selects: its index, or 0 when no entry won (the token
+// the pick writes for a request whose statistics hold no winner).
+__device__ __forceinline__ int key_token(unsigned long long key) {
+  return key == 0ull ? 0 : (int)(0xffffffffu - (uint32_t)key);
+}
+
+// Statistics slot (buf, b, chunk) of the two-buffer array.
+__device__ __forceinline__ ChunkStat* stat_slot(ChunkStat* stats, int buf,
+                                                int B, int b, int chunk) {
+  return stats + ((size_t)buf * B + b) * kMaxChunks + chunk;
+}
+
+// The merged statistics of request b over chunks 0..n_chunks-1, by one
+// whole warp: lane l merges chunks l, l+32, ... in that order, then a
+// butterfly combines the lanes (every lane returns the result).  Up to
+// kMergeBatch loads of a lane are issued before its first merge.
+constexpr int kMergeBatch = 8;
+__device__ __forceinline__ ChunkStat merge_row(const ChunkStat* row,
+                                               int n_chunks, int lane) {
+  ChunkStat st = empty_stat();
+  for (int c0 = lane; c0 < n_chunks; c0 += 32 * kMergeBatch) {
+    ChunkStat got[kMergeBatch];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (c0 + 32 * j < n_chunks) got[j] = row[c0 + 32 * j];
+#pragma unroll
+    for (int j = 0; j < kMergeBatch; ++j)
+      if (c0 + 32 * j < n_chunks) merge_stat(st, got[j]);
+  }
+  return warp_reduce_stat(st);
+}
+
 // --------------------------------------------------------------- bf16 load
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
   return __uint_as_float((uint32_t)b << 16);
 }
 
 // ------------------------------------------------------- workspace layout
-// Best-score hints: request b's words (one per position) start a 4 KB row
-// of their own.  Every CTA posts and reads them through a position; hints
-// packed into the same or nearby lines serialise at their L2 slices (4 KB
-// apart measured 2 us faster per position than 128 B apart).
-constexpr int kHintRowWords = 1024;
+// Decision keys of the tensor-core path: request b's keys (one per
+// position) start a 4 KB row of their own.  Every CTA posts and reads them
+// through a position; keys packed into the same or nearby lines serialise
+// at their L2 slices (4 KB apart measured 2 us faster per position than
+// 128 B apart).
+constexpr int kHintRowKeys = 512;
 
 struct WorkspaceLayout {
   size_t control;   // 256 B at offset 0: device error word and counters
-  size_t stats;     // [B, kMaxChunks] ChunkStat
+  size_t stats;     // [2, B, kMaxChunks] ChunkStat: two buffers, so that a
+                    // position's statistics survive the next position
   size_t rowstats;  // [B, K, 2] float (M, S)
-  size_t hints;     // [B] rows of kHintRowWords uint32; word k of row b is
-                    // the best decision score posted for (b, position k)
+  size_t hints;     // [B] rows of kHintRowKeys uint64; key k of row b is
+                    // the best decision key posted for (b, position k)
   size_t total;
 };
 
@@ -198,11 +253,11 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int B, int K) {
   L.control = off;
   off += 256;
   L.stats = off;
-  off = align_up(off + (size_t)B * kMaxChunks * sizeof(ChunkStat), 256);
+  off = align_up(off + 2 * (size_t)B * kMaxChunks * sizeof(ChunkStat), 256);
   L.rowstats = off;
   off = align_up(off + (size_t)B * K * 2 * sizeof(float), 256);
   L.hints = off;
-  off = align_up(off + (size_t)B * kHintRowWords * sizeof(uint32_t), 256);
+  off = align_up(off + (size_t)B * kHintRowKeys * sizeof(uint64_t), 256);
   L.total = off;
   return L;
 }
@@ -233,7 +288,7 @@ struct DraftArgs {
   float* probs;
   ChunkStat* stats;
   float* rowstats;
-  uint32_t* hints;  // [B] x kHintRowWords; words 0..K-1 zeroed per block
+  unsigned long long* hints;  // [B] x kHintRowKeys; keys 0..K-1 zeroed per block
   int* control;
 };
 
@@ -246,8 +301,11 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
                                cudaStream_t stream);
 // overlap_previous: launched with programmatic stream serialisation (the
 // kernel waits for the previous grid before reading its statistics).
-cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
-                        bool overlap_previous, cudaStream_t stream);
+// buf: the statistics buffer position k filled; from_keys: d_k is read from
+// the decision keys (tensor-core path) instead of the merged statistics.
+cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks, int buf,
+                        bool from_keys, bool overlap_previous,
+                        cudaStream_t stream);
 // Proposals of positions k_first .. k_first + k_count - 1.
 cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,
                              cudaStream_t stream);

@@ -14,25 +14,36 @@ namespace {
 
 constexpr int kPickThreads = 32;
 
-// One warp per request: merge the chunk statistics of position k (lane l
-// takes chunks l, l+32, ... in order, then a butterfly across the lanes),
-// write d_k and the row's (M, S).  When launched for programmatic dependent
-// launch it lets the next position's kernel be scheduled at once and waits
-// for the position kernel before reading its statistics.
+// One warp per request: merge the chunk statistics of position k from
+// buffer buf (merge_row's fixed order), write d_k and the row's (M, S).
+// On the tensor-core path (from_keys) d_k is the request's decision key,
+// the token the position kernels use; otherwise it is the merged winner,
+// and the row U[d_k] that the next position gathers first is prefetched
+// into L2.  When launched for programmatic dependent launch the kernel lets
+// the next kernel be scheduled at once and waits for the position kernel
+// before reading its statistics.
 __global__ void __launch_bounds__(kPickThreads)
-pick_kernel(DraftArgs a, int k, int n_chunks) {
+pick_kernel(DraftArgs a, int k, int n_chunks, int buf, bool from_keys) {
   sm100::launch_dependents();
   sm100::grid_dependency_wait();
   const int b = blockIdx.x;
-  ChunkStat st = empty_stat();
-  for (int c = threadIdx.x; c < n_chunks; c += kPickThreads)
-    merge_stat(st, a.stats[(size_t)b * kMaxChunks + c]);
-  st = warp_reduce_stat(st);
+  const ChunkStat st = merge_row(stat_slot(a.stats, buf, a.B, b, 0), n_chunks,
+                                 (int)threadIdx.x);
+  const int token = from_keys
+                        ? key_token(a.hints[(size_t)b * kHintRowKeys + k])
+                        : (st.idx == kNoIndex ? 0 : st.idx);
   if (threadIdx.x == 0) {
     const size_t row = (size_t)b * a.K + k;
-    a.tokens[row] = (st.idx == kNoIndex) ? 0 : st.idx;
+    a.tokens[row] = token;
     a.rowstats[2 * row] = st.m;
     a.rowstats[2 * row + 1] = st.s;
+  }
+  if (!from_keys && k + 1 < a.K) {
+    const size_t row_bytes = (size_t)a.r * (a.w_dtype == DSPARK_BF16 ? 2 : 4);
+    const char* u = static_cast<const char*>(a.U) + (size_t)token * row_bytes;
+    for (size_t off = (size_t)threadIdx.x * 128; off < row_bytes;
+         off += (size_t)kPickThreads * 128)
+      sm100::prefetch_l2(u + off);
   }
 }
 
@@ -110,8 +121,9 @@ __global__ void noise_words_kernel(uint64_t seed, uint64_t offset, int k,
 
 }  // namespace
 
-cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
-                        bool overlap_previous, cudaStream_t stream) {
+cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks, int buf,
+                        bool from_keys, bool overlap_previous,
+                        cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)a.B, 1, 1);
   cfg.blockDim = dim3(kPickThreads, 1, 1);
@@ -122,7 +134,7 @@ cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks,
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = overlap_previous ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, pick_kernel, a, k, n_chunks);
+  return cudaLaunchKernelEx(&cfg, pick_kernel, a, k, n_chunks, buf, from_keys);
 }
 
 cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,

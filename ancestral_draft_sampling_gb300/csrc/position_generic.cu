@@ -244,7 +244,7 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
     const int bl = warp + kWarps * i;
     if (bl >= nb) break;
     const ChunkStat red = warp_reduce_stat(st[i]);
-    if (lane == 0) a.stats[(size_t)(g0 + bl) * kMaxChunks + chunk] = red;
+    if (lane == 0) *stat_slot(a.stats, 0, a.B, g0 + bl, chunk) = red;
   }
 }
 

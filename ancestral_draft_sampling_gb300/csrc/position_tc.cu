@@ -18,26 +18,37 @@
 //                   tcgen05.mma kind::f16 (M = 128 vocab rows, N = B rounded
 //                   up to 16, K = r) into one of two TMEM accumulators.  A
 //                   (the Wb tile) is vocab-major, B (u) is r-major.
-//   warps 2..25     compute.  Warp (q, j), q = warp % 4, drains TMEM lanes
-//                   32q.. (vocab) of column group j (one sixth of the
-//                   requests) and writes l = base + bias (l = bias on padding
-//                   rows) into the tile buffer, in place.  After one barrier
-//                   the tile holds the float32 biased logits: one thread
-//                   stores it to global memory with a TMA tile store, and
-//                   compute warp w takes requests w, w+24, ... with lane L on
-//                   vocab 4L .. 4L+3 (one Philox block): scaled logits,
-//                   noise, the decision and the sum-exp, all from shared
-//                   memory.
+//   warps 2..9      drain.  Warp (q, h), q = warp % 4, drains TMEM lanes
+//                   32q.. (vocab) of the 16-column groups 2g+h (requests)
+//                   and writes l = base + bias (l = bias on padding rows)
+//                   into the tile buffer, in place; once all eight have, one
+//                   thread stores the tile to global memory with a TMA tile
+//                   store.  They drain tile t+1 while the decision warps
+//                   work on tile t.
+//   warps 10..31    decision.  Warp w takes requests w-10, w+12, ... with
+//                   lane L on vocab 4L .. 4L+3 (one Philox block): scaled
+//                   logits, noise, the decision and the sum-exp, all from
+//                   shared memory.
 // Decision: a conservative test per entry (one exp2, no logarithm) admits
 // every entry that may beat a reference score; only those get the exact
 // score s + g, merged over the warp by max/min reductions.  The reference
 // is the larger of the request's best score in this CTA and the best score
-// any CTA has posted for the request so far (an atomic maximum in global
-// memory, read once per tile): a score some entry reaches, so an entry
-// below it cannot win.  The same exp2 values, exp(s - reference), feed the
-// sum-exp, which is kept relative to the reference.  The Philox rounds
-// that depend only on the request's key and counter words are folded into
-// per-request constants.
+// any CTA has posted for the request so far: a score some entry reaches, so
+// an entry below it cannot win.  The posts are decision keys (the score's
+// order-preserving bits above the complement of the index) combined by an
+// atomic maximum in global memory and read once per tile.  The sum-exp
+// reuses the test's exp2 values, relative to a reference set from the data
+// alone.  The Philox rounds that depend only on the request's key and
+// counter words are folded into per-request constants.
+//
+// Once the grid has finished, the key of each request is the winner of the
+// position (largest score, lowest index on ties): the next position's
+// kernel reads d_{k-1} from it directly, so consecutive positions follow
+// each other with no kernel between them.  While its pipeline fills, that
+// kernel's decision warps also merge the previous position's per-chunk
+// statistics into tokens[:, k-1] and its softmax statistics (M, S); the
+// statistics alternate between two buffers, so position k never overwrites
+// those of position k-1.
 //
 // Every mbarrier wait is bounded; on a timeout the kernel records an error
 // in the workspace control word, stops issuing work, waits (bounded) for
@@ -66,6 +77,7 @@ constexpr int kWorkThreads = 32 * kWorkWarps;      // set-up and u gather
 constexpr int kDrainThreads = 32 * kDrainWarps;
 constexpr int kComputeThreads = 32 * kComputeWarps;
 constexpr int kMaxBpad = 96;
+constexpr int kGatherBatch = 4;                    // u pieces a thread loads at once
 constexpr int kMaxRows = (kMaxBpad + kComputeWarps - 1) / kComputeWarps;  // requests per compute warp
 constexpr uint32_t kTmemCols = 256;                // two accumulators
 constexpr uint32_t kAccCols = 128;
@@ -169,17 +181,6 @@ __device__ __forceinline__ float pick4(const float (&a)[4], int e) {
 template <bool kUnitT>
 __device__ __forceinline__ float scale(float l, float T) {
   return kUnitT ? l : __fdiv_rn(l, T);
-}
-
-// Float32 -> uint32 map that preserves order (for finite and infinite
-// values): flip every bit of negatives, set the sign bit of the others.
-__device__ __forceinline__ uint32_t ordered_bits(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float from_ordered_bits(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // Keeps the better of st and the warp's candidates (cb, ci): the largest
@@ -321,8 +322,9 @@ __device__ __forceinline__ void accumulate(RowState& st, const float (&f)[4]) {
                 kSumScale, st.sum);
 }
 
-// A best score posted by another CTA (order-preserving bits, 0 = none)
-// raises the reference of the candidate test.
+// A best score posted by another CTA (the order-preserving bits of a
+// decision key's score, 0 = none) raises the reference of the candidate
+// test.
 __device__ __forceinline__ void adopt_hint(RowState& st, uint32_t h) {
   if (h > ordered_bits(st.ref)) {
     st.ref = from_ordered_bits(h);
@@ -637,25 +639,46 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     // u row b = U[d_{k-1}(b)], stored r-major with the 128-byte swizzle: row
     // b of r-chunk c at c*(bpad*128) + b*128, 16-byte piece p at (p ^ (b & 7)).
     // d_{k-1} comes from the previous position's kernel: wait for it first.
+    // A thread issues the token loads of kGatherBatch pieces, then their U
+    // loads, then the stores: two memory round trips per batch.
     grid_dependency_wait();
     {
     const int ct = threadIdx.x - 64;
     const int pieces = a.r / 8;
+    const int total = P.bpad * pieces;
     const uint16_t* U = static_cast<const uint16_t*>(a.U);
-    for (int i = ct; i < P.bpad * pieces; i += kWorkThreads) {
-      const int b = i / pieces, piece = i - b * pieces;
-      const int c = piece >> 3, p = piece & 7;
-      uint4 val = make_uint4(0u, 0u, 0u, 0u);
-      if (b < a.B) {
-        int prev = (P.k == 0) ? a.d0[b] : a.tokens[(size_t)b * a.K + (P.k - 1)];
-        if ((unsigned)prev >= (unsigned)a.V) {
-          if (piece == 0) a.control[0] = kDevErrBadToken;
-          prev = 0;
-        }
-        val = __ldg(reinterpret_cast<const uint4*>(U + (size_t)prev * a.r) + piece);
+    for (int i0 = ct; i0 < total; i0 += kWorkThreads * kGatherBatch) {
+      int prev[kGatherBatch];
+#pragma unroll
+      for (int j = 0; j < kGatherBatch; ++j) {
+        const int i = i0 + j * kWorkThreads, b = i / pieces;
+        prev[j] = 0;
+        if (i < total && b < a.B)
+          prev[j] = (P.k == 0) ? a.d0[b]
+                               : key_token(a.hints[(size_t)b * kHintRowKeys + (P.k - 1)]);
       }
-      *reinterpret_cast<uint4*>(u_s + (size_t)c * (P.bpad * 128) + b * 128 +
-                                ((p ^ (b & 7)) << 4)) = val;
+      uint4 val[kGatherBatch];
+#pragma unroll
+      for (int j = 0; j < kGatherBatch; ++j) {
+        const int i = i0 + j * kWorkThreads, b = i / pieces, piece = i - b * pieces;
+        val[j] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < total && b < a.B) {
+          int pv = prev[j];
+          if ((unsigned)pv >= (unsigned)a.V) {
+            if (piece == 0) a.control[0] = kDevErrBadToken;
+            pv = 0;
+          }
+          val[j] = __ldg(reinterpret_cast<const uint4*>(U + (size_t)pv * a.r) + piece);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < kGatherBatch; ++j) {
+        const int i = i0 + j * kWorkThreads, b = i / pieces, piece = i - b * pieces;
+        const int c = piece >> 3, p = piece & 7;
+        if (i < total)
+          *reinterpret_cast<uint4*>(u_s + (size_t)c * (P.bpad * 128) + b * 128 +
+                                    ((p ^ (b & 7)) << 4)) = val[j];
+      }
     }
     }
     fence_proxy_async_smem();  // the MMA reads u through the async proxy
@@ -746,13 +769,12 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     } else {
     // ------------------------------------------------------------- compute
     const int cw = warp - 2 - kDrainWarps;
-    // lane i < kMaxRows: the best-score hint of this warp's row i (sampled
-    // requests only)
-    uint32_t* hint_ptr = nullptr;
+    // lane i < kMaxRows: the decision key of this warp's row i
+    unsigned long long* hint_ptr = nullptr;
     {
       const int hb = cw + kComputeWarps * lane;
-      if (lane < kMaxRows && hb < a.B && !(rows[hb].flags & kRowGreedy))
-        hint_ptr = a.hints + (size_t)hb * kHintRowWords + P.k;
+      if (lane < kMaxRows && hb < a.B)
+        hint_ptr = a.hints + (size_t)hb * kHintRowKeys + P.k;
     }
     uint32_t greedy_mask = 0;  // bit i: this warp's row i is greedy
 #pragma unroll
@@ -774,13 +796,29 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       rstate[lane] = make_float4(-INFINITY, -INFINITY, INFINITY,
                                  __int_as_float(kNoIndex));
     __syncwarp();
+    // the previous position, complete since grid_dependency_wait: d_{k-1}
+    // from its decision key and (M, S) from its merged statistics, one
+    // request per warp, while the first tile is still in flight
+    if (P.k > 0) {
+      for (int b = chunk + P.n_chunks * cw; b < a.B;
+           b += P.n_chunks * kComputeWarps) {
+        const ChunkStat ps = merge_row(
+            stat_slot(a.stats, (P.k - 1) & 1, a.B, b, 0), P.n_chunks, lane);
+        if (lane == 0) {
+          const size_t row = (size_t)b * a.K + (P.k - 1);
+          a.tokens[row] = key_token(a.hints[(size_t)b * kHintRowKeys + (P.k - 1)]);
+          a.rowstats[2 * row] = ps.m;
+          a.rowstats[2 * row + 1] = ps.s;
+        }
+      }
+    }
 
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       const uint32_t ph = (uint32_t)(t >> 1) & 1u;
       const int v0 = (t_begin + t) * kTileV;
       const float* tile = tiles + (size_t)buf * tile_floats;
-      const uint32_t hint_in = hint_ptr ? __ldcg(hint_ptr) : 0u;
+      const unsigned long long hint_in = hint_ptr ? __ldcg(hint_ptr) : 0ull;
       // the drain warps have written this tile's biased logits
       const bool ok = !*abort_flag && mbar_wait(&drained[buf], ph, kSpin);
       if (!ok && !*abort_flag) fail(kDevErrTimeout);
@@ -794,7 +832,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           float sv[4];
           scaled4<kUnitT>(l4, T, sv);
           const RowConst& rc = rows[b];
-          const uint32_t h = __shfl_sync(0xffffffffu, hint_in, i);
+          const uint32_t h = (uint32_t)(__shfl_sync(0xffffffffu, hint_in, i) >> 32);
           const float4 q = rstate[i];
           RowState st{sums[i], q.x, q.y, q.z, __float_as_int(q.w)};  // ref, sref, h, idx
           if ((greedy_mask >> i) & 1u) {
@@ -811,12 +849,15 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           sums[i] = st.sum;
           rstate[i] = make_float4(st.ref, st.sref, st.h, __int_as_float(st.idx));
         }
-        // post bests that beat the hint read for this tile
+        // post this CTA's own winners whose keys beat the key read for
+        // this tile (the one that ends the grid highest is the position's
+        // winner)
         __syncwarp();
-        uint32_t mine = 0;
+        unsigned long long mine = 0;
         if (lane < kMaxRows) {
           const float4 q = rstate[lane];
-          if (__float_as_int(q.w) != kNoIndex) mine = ordered_bits(q.x);
+          if (__float_as_int(q.w) != kNoIndex)
+            mine = decision_key(q.x, __float_as_int(q.w));
         }
         if (hint_ptr && mine > hint_in) atomicMax(hint_ptr, mine);
       }
@@ -839,7 +880,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         cs.best = cs.idx == kNoIndex ? -INFINITY : q.x;  // this CTA's own winner
         cs.m = q.y;  // the reference of the sum (-inf: none set)
         cs.s = sum;
-        a.stats[(size_t)b * kMaxChunks + chunk] = cs;
+        *stat_slot(a.stats, P.k & 1, a.B, b, chunk) = cs;
       }
     }
     }

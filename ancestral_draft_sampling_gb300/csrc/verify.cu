@@ -42,15 +42,6 @@ constexpr float kSlack = 1.000489f;   // 1 + 2^-11, rounded up
 // weights above e^57.
 constexpr float kMaxTestScore = 80.0f;
 
-__device__ __forceinline__ uint32_t ordered_bits(float f) {
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float from_ordered_bits(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 struct Best {
   float score;
   int idx;

@@ -343,8 +343,10 @@ def run_ours(args, rank, world):
         alg_bytes = position_kernel_bytes(w)
     elif dominant == "proposal":
         alg_bytes = 2 * B * K * V * 4
-    else:
-        alg_bytes = B * 1024 * 16
+    else:  # the pick reads one 16-byte statistic per (request, CTA)
+        n_ctas = min((V + 127) // 128,
+                     torch.cuda.get_device_properties(0).multi_processor_count)
+        alg_bytes = B * n_ctas * 16
     achieved = alg_bytes / (avg_ms[dominant] * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved,
                 "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
