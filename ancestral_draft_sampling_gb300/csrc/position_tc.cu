@@ -725,20 +725,36 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           for (int c0 = 16 * h; c0 < a.B; c0 += 32) {
             float bias[16];
             tmem_ld16(taddr + (uint32_t)c0, bias);  // within the 128 columns
-            tmem_ld_wait();
             const uint32_t pw =
                 (c0 < 32 ? pad0 : (c0 < 64 ? pad1 : pad2)) >> (c0 & 31);
+            if (c0 + 16 <= a.B) {
+              // all 16 requests present: the drafter logits are read while
+              // the TMEM load is in flight
+              float x[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int c = c0 + j;
-              if (c >= a.B) break;
-              float x;
-              if (kStaged)
-                x = __uint_as_float(
-                    (uint32_t)reinterpret_cast<const uint16_t*>(stage)[c * kTileV + m] << 16);
-              else
-                x = col[c * kTileV];
-              col[c * kTileV] = ((pw >> j) & 1u) ? bias[j] : __fadd_rn(x, bias[j]);
+              for (int j = 0; j < 16; ++j)
+                x[j] = kStaged ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(
+                                                     stage)[(c0 + j) * kTileV + m] << 16)
+                               : col[(c0 + j) * kTileV];
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                col[(c0 + j) * kTileV] =
+                    ((pw >> j) & 1u) ? bias[j] : __fadd_rn(x[j], bias[j]);
+            } else {
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int c = c0 + j;
+                if (c >= a.B) break;
+                float x;
+                if (kStaged)
+                  x = __uint_as_float(
+                      (uint32_t)reinterpret_cast<const uint16_t*>(stage)[c * kTileV + m] << 16);
+                else
+                  x = col[c * kTileV];
+                col[c * kTileV] = ((pw >> j) & 1u) ? bias[j] : __fadd_rn(x, bias[j]);
+              }
             }
           }
           // the ragged last tile: vocab rows past V become -inf, which no
