@@ -335,10 +335,9 @@ __device__ __forceinline__ void adopt_hint(RowState& st, uint32_t h) {
 
 // Steady state of a sampled request (its best is finite): the conservative
 // test for every entry, exact scores for the few that pass.
-__device__ __forceinline__ void sampled_step(const RowConst& rc,
+__device__ __forceinline__ void sampled_step(const uint4 w,
                                              const float (&s)[4], int v,
                                              RowState& st) {
-  const uint4 w = row_noise(rc, v);
   float f[4];
   sum_terms(st, s, f);
   const float h = st.h;
@@ -365,10 +364,9 @@ __device__ __forceinline__ float rough_score(float s, uint32_t x) {
 // First tile of a sampled request (nothing has won yet): each lane decides
 // its roughly best entry exactly, the warp keeps the best of those, then
 // the remaining entries go through the conservative test.
-__device__ __forceinline__ void sampled_first(const RowConst& rc,
+__device__ __forceinline__ void sampled_first(const uint4 w,
                                               const float (&s)[4], int v,
                                               RowState& st) {
-  const uint4 w = row_noise(rc, v);
   uint32_t first = 0;
   float top = -INFINITY;
 #pragma unroll
@@ -841,29 +839,41 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       if (ok && !*abort_flag) {
         const int v = v0 + 4 * lane;
 #pragma unroll
-        for (int i = 0; i < kMaxRows; ++i) {
-          const int b = cw + kComputeWarps * i;
-          if (b >= a.B) break;
-          const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
-          float sv[4];
-          scaled4<kUnitT>(l4, T, sv);
-          const RowConst& rc = rows[b];
-          const uint32_t h = (uint32_t)(__shfl_sync(0xffffffffu, hint_in, i) >> 32);
-          const float4 q = rstate[i];
-          RowState st{sums[i], q.x, q.y, q.z, __float_as_int(q.w)};  // ref, sref, h, idx
-          if ((greedy_mask >> i) & 1u) {
-            greedy_step(sv, v, st);
-          } else {
-            adopt_hint(st, h);
-            // first tile: bootstrap the reference; afterwards the steady
-            // state (which also handles a reference still at -inf)
-            if (t == 0 && st.ref == -INFINITY)
-              sampled_first(rc, sv, v, st);
-            else
-              sampled_step(rc, sv, v, st);
+        for (int i0 = 0; i0 < kMaxRows; i0 += 2) {
+          const int b0 = cw + kComputeWarps * i0;
+          if (b0 >= a.B) break;
+          const bool has1 = i0 + 1 < kMaxRows && b0 + kComputeWarps < a.B;
+          // the noise of two rows first: two independent Philox chains the
+          // scheduler interleaves (a row step is latency-bound; four chains
+          // spill at this kernel's 64 registers)
+          uint4 wn[2];
+          wn[0] = row_noise(rows[b0], v);
+          wn[1] = row_noise(rows[has1 ? b0 + kComputeWarps : b0], v);
+#pragma unroll
+          for (int i = i0; i < i0 + 2 && i < kMaxRows; ++i) {
+            const int b = cw + kComputeWarps * i;
+            if (b >= a.B) break;
+            const uint4 w = wn[i - i0];
+            const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
+            float sv[4];
+            scaled4<kUnitT>(l4, T, sv);
+            const uint32_t h = (uint32_t)(__shfl_sync(0xffffffffu, hint_in, i) >> 32);
+            const float4 q = rstate[i];
+            RowState st{sums[i], q.x, q.y, q.z, __float_as_int(q.w)};  // ref, sref, h, idx
+            if ((greedy_mask >> i) & 1u) {
+              greedy_step(sv, v, st);
+            } else {
+              adopt_hint(st, h);
+              // first tile: bootstrap the reference; afterwards the steady
+              // state (which also handles a reference still at -inf)
+              if (t == 0 && st.ref == -INFINITY)
+                sampled_first(w, sv, v, st);
+              else
+                sampled_step(w, sv, v, st);
+            }
+            sums[i] = st.sum;
+            rstate[i] = make_float4(st.ref, st.sref, st.h, __int_as_float(st.idx));
           }
-          sums[i] = st.sum;
-          rstate[i] = make_float4(st.ref, st.sref, st.h, __int_as_float(st.idx));
         }
         // post this CTA's own winners whose keys beat the key read for
         // this tile (the one that ends the grid highest is the position's
