@@ -7,7 +7,7 @@
 // softmax statistics out.  The pages keep the bias GEMM on cuBLAS; here it
 // is fused into the position kernel.
 //
-// Per CTA (one per SM, a contiguous range of 128-wide vocab tiles):
+// Per CTA (one per SM; CTA c takes the 128-wide vocab tiles c, c + grid, ...):
 //   warp 0, lane 0  TMA producer of Wb[r0:r0+64, v0:v0+128] stages (two
 //                   64x64 boxes, 128-byte swizzle) into a ring.
 //   warp 0, lane 1  TMA producer of the drafter-logit tile base[:, k,
@@ -457,9 +457,9 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   const DraftArgs& a = P.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x;
-  const int t_begin = (int)((long long)chunk * P.tiles_total / P.n_chunks);
-  const int t_end = (int)((long long)(chunk + 1) * P.tiles_total / P.n_chunks);
-  const int n_tiles = t_end - t_begin;
+  // tiles chunk, chunk + n_chunks, ...: at any moment the CTAs work on
+  // neighbouring tiles (measured faster than contiguous ranges)
+  const int n_tiles = (P.tiles_total - 1 - chunk) / P.n_chunks + 1;
   const int kchunks = a.r / kKChunk;
   const int tile_floats = P.bpad * kTileV;
 
@@ -531,7 +531,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       // -------------------------------------------------- Wb producer
       int g = 0;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t) {
-        const int v0 = (t_begin + t) * kTileV;
+        const int v0 = (chunk + t * P.n_chunks) * kTileV;
         for (int kc = 0; kc < kchunks; ++kc, ++g) {
           const int s = g % S;
           const uint32_t ph = (uint32_t)(g / S) & 1u;
@@ -556,7 +556,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       const uint32_t bytes = (uint32_t)(tile_floats * (int)sizeof(BT));
       int issued = 0;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t, ++issued) {
-        const int v0 = (t_begin + t) * kTileV;
+        const int v0 = (chunk + t * P.n_chunks) * kTileV;
         if (kStaged) {
           if (!mbar_wait(stage_free, ((uint32_t)t & 1u) ^ 1u, kSpin)) {
             fail(kDevErrTimeout);
@@ -702,7 +702,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       for (int t = 0; t < n_tiles; ++t) {
         const int buf = t & 1;
         const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-        const int v0 = (t_begin + t) * kTileV;
+        const int v0 = (chunk + t * P.n_chunks) * kTileV;
         float* tile = tiles + (size_t)buf * tile_floats;
         // bf16 logits arrive in the staging tile, so the f32 buffer is
         // written here: it must be released (tile t-2 read by the compute
@@ -830,7 +830,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     for (int t = 0; t < n_tiles; ++t) {
       const int buf = t & 1;
       const uint32_t ph = (uint32_t)(t >> 1) & 1u;
-      const int v0 = (t_begin + t) * kTileV;
+      const int v0 = (chunk + t * P.n_chunks) * kTileV;
       const float* tile = tiles + (size_t)buf * tile_floats;
       const unsigned long long hint_in = hint_ptr ? __ldcg(hint_ptr) : 0ull;
       // the drain warps have written this tile's biased logits
