@@ -79,9 +79,11 @@ typedef enum {
 /*
  * Bytes of device workspace dspark_draft_block needs for these sizes
  * (0 if the sizes are unsupported).  The workspace holds per-chunk softmax
- * statistics, per-row (max, sum-exp) of every position, the best-score hints
- * the position kernels share across CTAs, and a device error word.  Its contents need not be initialised and are overwritten by each
- * call; two calls in flight at the same time must not share a workspace.
+ * statistics (two buffers, so consecutive positions do not overwrite each
+ * other's), per-row (max, sum-exp) of every position, the decision keys the
+ * position kernels share across CTAs, and a device error word.  Its
+ * contents need not be initialised and are overwritten by each call; two
+ * calls in flight at the same time must not share a workspace.
  */
 DSPARK_API size_t dspark_draft_workspace_bytes(int B, int K, int V, int r);
 
@@ -204,8 +206,10 @@ DSPARK_API size_t dspark_draft_host_workspace_bytes(int B, int K, int V, int r);
  *                drafter-logit copies (must differ from stream).
  * Position k's drafter logits (B rows of V values, one 2-D copy) travel on
  * copy_stream while earlier positions compute on stream.  Position k waits
- * for its own copy only, and its proposals are written right after its pick,
- * so the block's work hides behind the copies.  The copies start after all
+ * for its own copy only, and each position's proposals are written as soon
+ * as its softmax statistics exist (after the next position on the
+ * tensor-core path, after its pick otherwise), so the block's work hides
+ * behind the copies.  The copies start after all
  * work issued to `stream` before the call.  Outputs are identical to
  * dspark_draft_block's.  Host buffers must stay valid until `stream` has
  * passed the end of the call.  The call creates and destroys K+1 CUDA
