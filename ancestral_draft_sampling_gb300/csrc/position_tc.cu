@@ -391,6 +391,17 @@ __device__ __forceinline__ void sampled_first(const uint4 w,
   accumulate(st, f);
 }
 
+// sampled_first out of line: it runs once per request and CTA, and inlined
+// into every row of the unrolled row loop it made the kernel's code large
+// enough to slow the steady state (measured 5 us per block).  Arguments and
+// result go by value, so the caller's arrays stay in registers.
+__device__ __noinline__ RowState sampled_first_call(const uint4 w, const float4 s4,
+                                                    int v, RowState st) {
+  const float s[4] = {s4.x, s4.y, s4.z, s4.w};
+  sampled_first(w, s, v, st);
+  return st;
+}
+
 // A greedy request: no noise; an entry is a candidate iff s > best.
 __device__ __forceinline__ void greedy_step(const float (&s)[4], int v,
                                             RowState& st) {
@@ -867,7 +878,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
               // first tile: bootstrap the reference; afterwards the steady
               // state (which also handles a reference still at -inf)
               if (t == 0 && st.ref == -INFINITY)
-                sampled_first(w, sv, v, st);
+                st = sampled_first_call(w, make_float4(sv[0], sv[1], sv[2], sv[3]), v, st);
               else
                 sampled_step(w, sv, v, st);
             }
