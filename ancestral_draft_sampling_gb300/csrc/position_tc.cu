@@ -920,6 +920,19 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         *stat_slot(a.stats, P.k & 1, a.B, b, chunk) = cs;
       }
     }
+    // the next position first gathers U[d_k]: bring the rows of this CTA's
+    // own winners into L2 (the position's winner is one of them)
+    if (P.k + 1 < a.K) {
+      const int row_bytes = a.r * 2;  // bf16 U
+#pragma unroll
+      for (int i = 0; i < kMaxRows; ++i) {
+        const int b = cw + kComputeWarps * i;
+        if (b >= a.B) break;
+        const int idx = __float_as_int(rstate[i].w);
+        if (idx != kNoIndex && lane * 128 < row_bytes)
+          prefetch_l2(static_cast<const char*>(a.U) + (size_t)idx * row_bytes + lane * 128);
+      }
+    }
     }
   }
 
