@@ -55,6 +55,61 @@ __device__ __forceinline__ uint4 noise_block(uint64_t seed, uint64_t offset,
   return philox4x32_10(ctr, key);
 }
 
+// One Philox4x32-10 round (the published multipliers) with round key k.
+__device__ __forceinline__ uint4 philox_round(uint4 c, uint32_t k0, uint32_t k1) {
+  const unsigned long long pa = (unsigned long long)0xD2511F53u * c.x;
+  const unsigned long long pb = (unsigned long long)0xCD9E8D57u * c.z;
+  return make_uint4((uint32_t)(pb >> 32) ^ c.y ^ k0, (uint32_t)pb,
+                    (uint32_t)(pa >> 32) ^ c.w ^ k1, (uint32_t)pa);
+}
+
+// Philox4x32-10 along a row of counters (x0, c1, c2, c3) with only x0
+// varying, under key (k0, k1).  The parts of rounds 1 and 2 that depend on
+// the fixed words alone fold into constants: round 1 gives
+// (A, B, hi(M0 x0) ^ C1, lo(M0 x0)) with A = hi(M1 c2) ^ c1 ^ k0,
+// B = lo(M1 c2), C1 = c3 ^ k1; round 2 then gives
+// (hi(M1 z) ^ D2, lo(M1 z), lo(M0 x0) ^ E2, F2) with z the third word,
+// D2 = B ^ k0', E2 = hi(M0 A) ^ k1', F2 = lo(M0 A).  philox_fold computes
+// pre = (C1, D2, E2, F2) and the round keys of rounds 3..10 (round r uses
+// (k0 + r W0, k1 + r W1), r = 0..9); philox_folded gives the block of x0,
+// bit-identical to philox4x32_10.
+__device__ __forceinline__ void philox_fold(uint4& pre, uint4 (&rk)[4],
+                                            uint32_t k0, uint32_t k1,
+                                            uint32_t c1, uint32_t c2,
+                                            uint32_t c3) {
+  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+  const unsigned long long m1c2 = (unsigned long long)0xCD9E8D57u * c2;
+  const uint32_t A = (uint32_t)(m1c2 >> 32) ^ c1 ^ k0;
+  const uint32_t Bv = (uint32_t)m1c2;
+  const uint32_t C1 = c3 ^ k1;
+  const unsigned long long m0a = (unsigned long long)0xD2511F53u * A;
+  pre = make_uint4(C1, Bv ^ (k0 + W0), (uint32_t)(m0a >> 32) ^ (k1 + W1),
+                   (uint32_t)m0a);
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t r = 2 * j + 2;
+    rk[j] = make_uint4(k0 + r * W0, k1 + r * W1, k0 + (r + 1) * W0,
+                       k1 + (r + 1) * W1);
+  }
+}
+
+__device__ __forceinline__ uint4 philox_folded(const uint4& pre_ref,
+                                               const uint4 (&rk)[4],
+                                               uint32_t x0) {
+  const uint4 pre = pre_ref;
+  const unsigned long long pa = (unsigned long long)0xD2511F53u * x0;
+  const uint32_t z = (uint32_t)(pa >> 32) ^ pre.x;
+  const unsigned long long pb = (unsigned long long)0xCD9E8D57u * z;
+  uint4 c = make_uint4((uint32_t)(pb >> 32) ^ pre.y, (uint32_t)pb,
+                       (uint32_t)pa ^ pre.z, pre.w);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint4 k = rk[j];
+    c = philox_round(c, k.x, k.y);
+    c = philox_round(c, k.z, k.w);
+  }
+  return c;
+}
+
 __device__ __forceinline__ uint32_t word_of(uint4 w, int i) {
   return i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w;
 }

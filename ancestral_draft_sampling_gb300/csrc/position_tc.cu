@@ -205,56 +205,18 @@ __device__ __forceinline__ void warp_take_best(RowState& st, float cb, int ci) {
   }
 }
 
-// One Philox4x32-10 round (the published multipliers) with round key k.
-__device__ __forceinline__ uint4 philox_round(uint4 c, uint32_t k0, uint32_t k1) {
-  const unsigned long long pa = (unsigned long long)0xD2511F53u * c.x;
-  const unsigned long long pb = (unsigned long long)0xCD9E8D57u * c.z;
-  return make_uint4((uint32_t)(pb >> 32) ^ c.y ^ k0, (uint32_t)pb,
-                    (uint32_t)(pa >> 32) ^ c.w ^ k1, (uint32_t)pa);
-}
-
 // The noise block of vocab v: Philox4x32-10 of counter (v >> 2, c1, c2, c3)
-// under the request's key.  Only counter word 0 varies along a row, so the
-// parts of rounds 1 and 2 that depend on the other words alone are
-// per-request constants (row_constants): round 1 gives
-// (A, B, hi(M0 x0) ^ C1, lo(M0 x0)) with A = hi(M1 c2) ^ c1 ^ k0,
-// B = lo(M1 c2), C1 = c3 ^ k1; round 2 then gives
-// (hi(M1 z) ^ D2, lo(M1 z), lo(M0 x0) ^ E2, F2) with z the third word,
-// D2 = B ^ k0', E2 = hi(M0 A) ^ k1', F2 = lo(M0 A).
+// under the request's key, from the request's folded constants.
 __device__ __forceinline__ uint4 row_noise(const RowConst& rc, int v) {
-  const uint4 pre = rc.pre;
-  const unsigned long long pa = (unsigned long long)0xD2511F53u * ((uint32_t)v >> 2);
-  const uint32_t z = (uint32_t)(pa >> 32) ^ pre.x;
-  const unsigned long long pb = (unsigned long long)0xCD9E8D57u * z;
-  uint4 c = make_uint4((uint32_t)(pb >> 32) ^ pre.y, (uint32_t)pb,
-                       (uint32_t)pa ^ pre.z, pre.w);
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const uint4 k = rc.rk[j];
-    c = philox_round(c, k.x, k.y);
-    c = philox_round(c, k.z, k.w);
-  }
-  return c;
+  return philox_folded(rc.pre, rc.rk, (uint32_t)v >> 2);
 }
 
-// Per-request constants of row_noise for key (k0, k1) and counter words
-// c1, c2, c3 (round r uses key (k0 + r W0, k1 + r W1), r = 0..9).
+// The folded constants of a request with key (k0, k1) and counter words
+// c1, c2, c3.
 __device__ __forceinline__ void row_constants(RowConst& rc, uint32_t k0,
                                               uint32_t k1, uint32_t c1,
                                               uint32_t c2, uint32_t c3) {
-  const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
-  const unsigned long long m1c2 = (unsigned long long)0xCD9E8D57u * c2;
-  const uint32_t A = (uint32_t)(m1c2 >> 32) ^ c1 ^ k0;
-  const uint32_t Bv = (uint32_t)m1c2;
-  const uint32_t C1 = c3 ^ k1;
-  const unsigned long long m0a = (unsigned long long)0xD2511F53u * A;
-  rc.pre = make_uint4(C1, Bv ^ (k0 + W0), (uint32_t)(m0a >> 32) ^ (k1 + W1),
-                      (uint32_t)m0a);
-  for (int j = 0; j < 4; ++j) {
-    const uint32_t r = 2 * j + 2;
-    rc.rk[j] = make_uint4(k0 + r * W0, k1 + r * W1, k0 + (r + 1) * W0,
-                          k1 + (r + 1) * W1);
-  }
+  philox_fold(rc.pre, rc.rk, k0, k1, c1, c2, c3);
 }
 
 // Exact decision scores of the sampled entries in `cand`, merged into st.

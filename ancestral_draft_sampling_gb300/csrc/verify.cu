@@ -101,8 +101,8 @@ __device__ __forceinline__ void load_block(const float* __restrict__ p,
 // the candidates, warp merge.  Warp-uniform control flow.
 __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
                                             float4 pv, float4 qv, bool resid,
-                                            uint64_t seed, uint64_t offset,
-                                            int pos) {
+                                            const uint4& pre,
+                                            const uint4 (&rk)[4]) {
   float wt[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -111,7 +111,7 @@ __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
     wt[e] = d > 0.0f ? d : 0.0f;  // NaN and non-positive weights: 0
     any |= wt[e] > 0.0f;
   }
-  const uint4 w = noise_block(seed, offset, pos, kNoiseResample, (uint32_t)j);
+  const uint4 w = philox_folded(pre, rk, (uint32_t)j);
   // 2^32 (1 + slack) e^-best; +inf (everything is a candidate) while nothing
   // has won or e^-best is out of float32's normal range
   const float c = (st.idx == kNoIndex || st.score > kMaxTestScore)
@@ -141,12 +141,13 @@ __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
 
 // Gumbel-max over log(weight) on this CTA's slice [lo, hi) of Philox blocks,
 // weights max(p - q, 0) when q != nullptr (the residual), else p; zero
-// weights never win.  Then the cluster-wide winner and "some weight was
+// weights never win.  (pre, rk): the folded Philox constants of noise
+// stream 2 at the drawing position (philox_fold).  Then the cluster-wide winner and "some weight was
 // positive", identical in every CTA of the cluster.
 template <bool kVec>
 __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p,
                          const float* __restrict__ q, int V, int lo, int hi,
-                         uint64_t seed, uint64_t offset, int pos, Best* part,
+                         const uint4& pre, const uint4 (&rk)[4], Best* part,
                          int* any_part, Slot* slot) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool resid = q != nullptr;
@@ -159,9 +160,9 @@ __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p
     float4 p0, q0, p1, q1;
     load_block<kVec>(p, q, V, j0, hi, p0, q0);
     load_block<kVec>(p, q, V, j1, hi, p1, q1);
-    sweep_block(st, any, j0, p0, q0, resid, seed, offset, pos);
+    sweep_block(st, any, j0, p0, q0, resid, pre, rk);
     if (base + kStride < hi)
-      sweep_block(st, any, j1, p1, q1, resid, seed, offset, pos);
+      sweep_block(st, any, j1, p1, q1, resid, pre, rk);
   }
   any = __any_sync(0xffffffffu, any);
   if (lane == 0) {
@@ -203,6 +204,7 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
   __shared__ Best part[kVerifyWarps];
   __shared__ int any_part[kVerifyWarps];
   __shared__ Slot slot;
+  __shared__ uint4 s_pre, s_rk[4];
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -233,16 +235,21 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
     return;
   }
   const int kk = s_first;
+  if (threadIdx.x == 0)
+    philox_fold(s_pre, s_rk, (uint32_t)sd, (uint32_t)(sd >> 32),
+                (uint32_t)kk | ((uint32_t)kNoiseResample << 16), (uint32_t)off,
+                (uint32_t)(off >> 32));
+  __syncthreads();
   const float* prow = p + ((size_t)b * (K + 1) + kk) * V;
   const float* qrow = kk < K ? q + ((size_t)b * K + kk) * V : nullptr;
   // this CTA's slice of the row's Philox blocks
   const int n_blk = (V + 3) / 4;
   const int per = (n_blk + C - 1) / C;
   const int lo = min(rank * per, n_blk), hi = min(lo + per, n_blk);
-  Slot r = draw_row<kVec>(cluster, prow, qrow, V, lo, hi, sd, off, kk, part,
+  Slot r = draw_row<kVec>(cluster, prow, qrow, V, lo, hi, s_pre, s_rk, part,
                           any_part, &slot);
   if (qrow != nullptr && !r.any)  // residual all zero: draw from p itself
-    r = draw_row<kVec>(cluster, prow, nullptr, V, lo, hi, sd, off, kk, part,
+    r = draw_row<kVec>(cluster, prow, nullptr, V, lo, hi, s_pre, s_rk, part,
                        any_part, &slot);
   if (rank == 0 && threadIdx.x == 0) {
     accepted_len[b] = kk;

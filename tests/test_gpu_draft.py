@@ -146,6 +146,31 @@ def test_greedy_ties_lowest_index():
     assert probs[0, 0, 17] == 1.0 and probs[0, 0].sum() == 1.0
 
 
+def test_greedy_ties_across_ctas_tensor_core():
+    # The tensor-core kernel combines the CTAs' winners through 64-bit
+    # decision keys (score bits above the complement of the index): equal
+    # maxima held by different CTAs must resolve to the lowest index.  With
+    # 313 tiles over the CTAs, tile t belongs to CTA t mod grid, so index
+    # 20000 (tile 156) is reached before index 129 (tile 1) is finished.
+    B, K, V, r = 6, 3, 40000, 64
+    w = wl.make_custom(B, K, V, r, seed=21, base_dtype=wl.F32,
+                       w_dtype=wl.BF16, w_std=0.0, greedy_rows=list(range(B)))
+    w.base[:] = -1.0
+    w.base[0, :, [39000, 20000, 129]] = 3.0   # three CTAs -> 129
+    w.base[1, :, :] = 0.5                      # every CTA ties -> 0
+    w.base[2, :, [6, 5]] = 2.0                 # one warp -> 5
+    w.base[3, :, [39999, 39998, 38000]] = 7.0  # last tiles -> 38000
+    w.base[4, 0, 777] = 4.0                    # a single maximum
+    w.base[4, 1:, [31000, 30999]] = 4.0        # -> 30999
+    w.base[5, :, 1:] = -np.inf                 # only index 0 finite -> 0
+    tokens, logits, probs = _np(run_draft(w))
+    ref = oracle.draft_block(w.base, w.U, w.Wb, w.d0, w.seed, w.offset, w.T,
+                             greedy=w.greedy)
+    np.testing.assert_array_equal(tokens, ref.tokens)
+    assert list(tokens[:, 0]) == [129, 0, 5, 38000, 777, 0]
+    assert (probs.sum(axis=2) == 1.0).all()   # one-hot proposals
+
+
 def test_nan_valid_row_gives_legal_token():
     w = wl.make_custom(2, 2, 900, 16, seed=4)
     w.base[0, 0, ::3] = np.nan
