@@ -14,7 +14,9 @@ Parity status: every oracle function is pinned by ``tests/test_oracle_pins.py``
 (Philox known answers and cuRAND's host generator, the Gumbel CDF, chi-square
 of Gumbel-max against the closed-form softmax, conditioning, the greedy chain
 against numpy's argmax, the bias against a float64 GEMV, proposal sums, and
-losslessness of standard verification).
+losslessness of standard verification) and ``tests/test_oracle_block.py``
+(block verification: losslessness by chi-square, its reduction to the
+standard rule at K = 1, identical draft and target).
 """
 from __future__ import annotations
 
@@ -76,6 +78,9 @@ def _load():
         lib.oracle_verify_standard.argtypes = [P, P, P, P, P, I, I, I, P, P,
                                                P, P]
         lib.oracle_verify_standard.restype = I
+        lib.oracle_verify_block.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P,
+                                            P, P]
+        lib.oracle_verify_block.restype = I
         _lib = lib
         return lib
 
@@ -220,7 +225,7 @@ def draft_chains(base, U, Wb, d0, seed, offset, T, depth, greedy=None,
 
 
 class VerifyResult:
-    __slots__ = ("accepted_len", "emitted", "top2")
+    __slots__ = ("accepted_len", "emitted", "top2", "h", "eta")
 
 
 def verify_standard(draft_probs, target_probs, tokens, seed, offset) -> VerifyResult:
@@ -243,4 +248,34 @@ def verify_standard(draft_probs, target_probs, tokens, seed, offset) -> VerifyRe
                                     _ptr(scratch))
     if rc != 0:
         raise ValueError("oracle_verify_standard rejected its arguments")
+    return out
+
+
+def verify_block(draft_probs, target_probs, tokens, seed, offset) -> VerifyResult:
+    """Block verification (PR #21, "2. Golden sampling semantics": the
+    ``block`` rejection_sample_method, Sun et al. 2024), see
+    oracle_verify_block.  Besides accepted_len, emitted and top2 the result
+    holds ``h`` [B,K] (float64: the thresholds h_1..h_K) and ``eta`` [B,K]
+    (float32: the uniforms they are compared with)."""
+    lib = _load()
+    B, K, V = draft_probs.shape
+    assert target_probs.shape == (B, K + 1, V)
+    q = np.ascontiguousarray(draft_probs, dtype=np.float32)
+    p = np.ascontiguousarray(target_probs, dtype=np.float32)
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    s = np.ascontiguousarray(seed, dtype=np.uint64)
+    o = np.ascontiguousarray(offset, dtype=np.uint64)
+    out = VerifyResult()
+    out.accepted_len = np.zeros(B, dtype=np.int32)
+    out.emitted = np.zeros(B, dtype=np.int32)
+    out.top2 = np.zeros((B, 2), dtype=np.float32)
+    out.h = np.zeros((B, K), dtype=np.float64)
+    out.eta = np.zeros((B, K), dtype=np.float32)
+    scratch = np.empty(V, dtype=np.float32)
+    rc = lib.oracle_verify_block(_ptr(q), _ptr(p), _ptr(t), _ptr(s), _ptr(o),
+                                 B, K, V, _ptr(out.accepted_len),
+                                 _ptr(out.emitted), _ptr(out.top2),
+                                 _ptr(out.h), _ptr(out.eta), _ptr(scratch))
+    if rc != 0:
+        raise ValueError("oracle_verify_block rejected its arguments")
     return out

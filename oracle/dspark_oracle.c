@@ -23,7 +23,8 @@
  *     padding rows draw from the bias alone.  Results table: the Markov head
  *     is rank 256 ("rank-256 Markov head").
  *   brb-nv/TensorRT-LLM PR #21, "2. Golden sampling semantics": the default
- *     verification rule is standard token-level rejection sampling.
+ *     verification rule is standard token-level rejection sampling; the
+ *     block rule is the block verification of Sun et al. (2024).
  *
  * Readings where the pages are silent (each is listed in the design doc):
  *   - Philox variant: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
@@ -353,6 +354,101 @@ int oracle_verify_standard(const float* draft_probs, const float* target_probs,
       emit = gumbel_max_weights(pK, V, seed[b], offset[b], K, &best, &second);
     }
     accepted_len[b] = acc;
+    emitted[b] = emit < 0 ? 0 : emit;
+    if (emit_top2) {
+      emit_top2[2 * b] = best;
+      emit_top2[2 * b + 1] = second;
+    }
+  }
+  return 0;
+}
+
+/* ----------------------------------------------------- block verification */
+
+/*
+ * Block verification: the block value of rejection_sample_method in PR #21,
+ * "2. Golden sampling semantics", which the pages identify as the block
+ * verification of Sun et al. (2024) and test for losslessness by chi-square
+ * (Test Coverage).  The pages name the rule only; this is the published
+ * algorithm restated, with
+ * 0-based positions (q_k = draft_probs[b,k], p_k = target_probs[b,k],
+ * d_k = tokens[b,k]):
+ *
+ *   w_0 = 1;  w_{k+1} = min(w_k * (p_k[d_k] / q_k[d_k]), 1)   (k = 0..K-1)
+ *   for i = 1..K-1:  r_i = sum_x max(w_i p_i(x) - q_i(x), 0)
+ *                    h_i = r_i / (r_i + 1 - w_i)   (1 when r_i = 1 - w_i = 0)
+ *   h_K = w_K
+ *   accepted_len tau = the largest i in 1..K with eta_i <= h_i (0 if none),
+ *   eta_i the stream-1 uniform of position i-1 (the standard rule's u_{i-1});
+ *   emitted: drawn from p_K when tau = K, else from norm(max(w_tau p_tau -
+ *   q_tau, 0)) (from p_tau if that is all zero), by Gumbel-max with stream-2
+ *   noise at position tau.
+ *
+ * Arithmetic: the w chain and every per-entry term in float32 (a quotient,
+ * a product, a difference, each rounded once; a NaN w or term counts as 0);
+ * the sums r_i and h_i in double.  h_out [B,K] (or NULL) receives h_1..h_K,
+ * eta_out [B,K] (or NULL) eta_1..eta_K.  Returns 0, or -1 on a bad argument.
+ */
+int oracle_verify_block(const float* draft_probs, const float* target_probs,
+                        const int32_t* tokens, const uint64_t* seed,
+                        const uint64_t* offset, int B, int K, int V,
+                        int32_t* accepted_len, int32_t* emitted,
+                        float* emit_top2, double* h_out, float* eta_out,
+                        float* residual_scratch) {
+  if (B <= 0 || K <= 0 || V <= 0) return -1;
+  for (int b = 0; b < B; ++b) {
+    const float* qb = draft_probs + (size_t)b * K * (size_t)V;
+    const float* pb = target_probs + (size_t)b * (K + 1) * (size_t)V;
+    /* w_0 .. w_K */
+    float w[65];
+    if (K > 64) return -1;
+    w[0] = 1.0f;
+    for (int k = 0; k < K; ++k) {
+      int d = tokens[(size_t)b * K + k];
+      if (d < 0 || d >= V) return -1;
+      float ratio = pb[(size_t)k * V + d] / qb[(size_t)k * V + d];
+      float t = w[k] * ratio;
+      w[k + 1] = t < 1.0f ? t : (t >= 1.0f ? 1.0f : 0.0f); /* NaN -> 0 */
+    }
+    int tau = 0;
+    for (int i = 1; i <= K; ++i) {
+      double h;
+      if (i < K) {
+        const float* p = pb + (size_t)i * V;
+        const float* q = qb + (size_t)i * V;
+        double r = 0.0;
+        for (int x = 0; x < V; ++x) {
+          float term = w[i] * p[x] - q[x];
+          if (term > 0.0f) r += (double)term;
+        }
+        double den = r + (1.0 - (double)w[i]);
+        h = den > 0.0 ? r / den : 1.0;
+      } else {
+        h = (double)w[K];
+      }
+      float eta = oracle_accept_uniform(
+          oracle_noise_word(seed[b], offset[b], i - 1, 1, 0u));
+      if ((double)eta <= h) tau = i;
+      if (h_out) h_out[(size_t)b * K + (i - 1)] = h;
+      if (eta_out) eta_out[(size_t)b * K + (i - 1)] = eta;
+    }
+    int emit;
+    float best = -INFINITY, second = -INFINITY;
+    const float* p = pb + (size_t)tau * V;
+    if (tau == K) {
+      emit = gumbel_max_weights(p, V, seed[b], offset[b], K, &best, &second);
+    } else {
+      const float* q = qb + (size_t)tau * V;
+      int any = 0;
+      for (int x = 0; x < V; ++x) {
+        float term = w[tau] * p[x] - q[x];
+        residual_scratch[x] = term > 0.0f ? term : 0.0f;
+        if (residual_scratch[x] > 0.0f) any = 1;
+      }
+      emit = gumbel_max_weights(any ? residual_scratch : p, V, seed[b],
+                                offset[b], tau, &best, &second);
+    }
+    accepted_len[b] = tau;
     emitted[b] = emit < 0 ? 0 : emit;
     if (emit_top2) {
       emit_top2[2 * b] = best;
