@@ -16,7 +16,7 @@ from . import _lib
 from ._lib import BF16, F32, DsparkError  # noqa: F401
 
 __all__ = ["draft_block", "draft_block_noalloc", "draft_block_profile",
-           "draft_block_host", "HostWorkspace", "verify_standard",
+           "draft_block_host", "HostWorkspace", "verify_standard", "verify_block",
            "noise_words", "workspace_bytes", "read_device_error",
            "DraftWorkspace", "DsparkError", "F32", "BF16", "version"]
 
@@ -211,9 +211,8 @@ def draft_block_profile(base_logits, U, Wb, d0, seed, offset, T: float, *,
     return {names[i]: (float(ms[i]), int(n[i])) for i in range(3)}
 
 
-def verify_standard(draft_probs, target_probs, tokens, seed, offset, *,
-                    accepted_len=None, emitted_token=None, stream=None):
-    """Standard rejection verification.  Returns (accepted_len, emitted)."""
+def _verify(fn, draft_probs, target_probs, tokens, seed, offset,
+            accepted_len, emitted_token, stream):
     torch = _torch()
     B, K, V = draft_probs.shape
     if tuple(target_probs.shape) != (B, K + 1, V):
@@ -223,12 +222,27 @@ def verify_standard(draft_probs, target_probs, tokens, seed, offset, *,
         accepted_len = torch.empty(B, dtype=torch.int32, device=dev)
     if emitted_token is None:
         emitted_token = torch.empty(B, dtype=torch.int32, device=dev)
-    st = _lib.load().dspark_verify_standard(
+    st = getattr(_lib.load(), fn)(
         _ptr(draft_probs), _ptr(target_probs), _ptr(tokens), _ptr(seed),
         _ptr(offset), B, K, V, _ptr(accepted_len), _ptr(emitted_token),
         _stream(stream))
-    _lib.check("dspark_verify_standard", st)
+    _lib.check(fn, st)
     return accepted_len, emitted_token
+
+
+def verify_standard(draft_probs, target_probs, tokens, seed, offset, *,
+                    accepted_len=None, emitted_token=None, stream=None):
+    """Standard rejection verification.  Returns (accepted_len, emitted)."""
+    return _verify("dspark_verify_standard", draft_probs, target_probs, tokens,
+                   seed, offset, accepted_len, emitted_token, stream)
+
+
+def verify_block(draft_probs, target_probs, tokens, seed, offset, *,
+                 accepted_len=None, emitted_token=None, stream=None):
+    """Block verification (same arguments and outputs as verify_standard).
+    Returns (accepted_len, emitted)."""
+    return _verify("dspark_verify_block", draft_probs, target_probs, tokens,
+                   seed, offset, accepted_len, emitted_token, stream)
 
 
 def noise_words(seed: int, offset: int, k: int, stream_id: int, n: int,

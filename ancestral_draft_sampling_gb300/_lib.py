@@ -33,6 +33,7 @@ EXPORTED = (
     "dspark_draft_host_workspace_bytes",
     "dspark_draft_block_host",
     "dspark_verify_standard",
+    "dspark_verify_block",
     "dspark_noise_words",
     "dspark_read_device_error",
     "dspark_status_string",
@@ -84,6 +85,8 @@ def load() -> ctypes.CDLL:
         lib.dspark_draft_block_host.restype = I
         lib.dspark_verify_standard.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
         lib.dspark_verify_standard.restype = I
+        lib.dspark_verify_block.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
+        lib.dspark_verify_block.restype = I
         lib.dspark_noise_words.argtypes = [U64, U64, I, I, I, P, P, P]
         lib.dspark_noise_words.restype = I
         lib.dspark_read_device_error.argtypes = [P, P, P]

@@ -289,6 +289,27 @@ cudaError_t noalloc_scratch(void** out) {
   return cudaSuccess;
 }
 
+// The argument checks and launch shared by the two verification rules.
+dspark_status verify_rule(const float* draft_probs, const float* target_probs,
+                          const int32_t* tokens, const uint64_t* seed,
+                          const uint64_t* offset, int B, int K, int V,
+                          int32_t* accepted_len, int32_t* emitted_token,
+                          bool block, cudaStream_t stream) {
+  if (B <= 0 || K <= 0 || V <= 0) return DSPARK_ERR_INVALID_ARG;
+  if (!draft_probs || !target_probs || !tokens || !seed || !offset ||
+      !accepted_len || !emitted_token)
+    return DSPARK_ERR_INVALID_ARG;
+  const void* ptrs[] = {draft_probs, target_probs, tokens, seed,
+                        offset, accepted_len, emitted_token};
+  for (const void* p : ptrs)
+    if (!aligned16(p)) return DSPARK_ERR_INVALID_ARG;
+  if (B > 65535 || K > DSPARK_MAX_K || V > DSPARK_MAX_V)
+    return DSPARK_ERR_UNSUPPORTED;
+  return from_cuda(launch_verify(draft_probs, target_probs, tokens, seed,
+                                 offset, B, K, V, accepted_len, emitted_token,
+                                 sm_count(), block, stream));
+}
+
 }  // namespace
 
 extern "C" {
@@ -471,19 +492,18 @@ dspark_status dspark_verify_standard(const float* draft_probs,
                                      int V, int32_t* accepted_len,
                                      int32_t* emitted_token,
                                      cudaStream_t stream) {
-  if (B <= 0 || K <= 0 || V <= 0) return DSPARK_ERR_INVALID_ARG;
-  if (!draft_probs || !target_probs || !tokens || !seed || !offset ||
-      !accepted_len || !emitted_token)
-    return DSPARK_ERR_INVALID_ARG;
-  const void* ptrs[] = {draft_probs, target_probs, tokens, seed,
-                        offset, accepted_len, emitted_token};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return DSPARK_ERR_INVALID_ARG;
-  if (B > 65535 || K > DSPARK_MAX_K || V > DSPARK_MAX_V)
-    return DSPARK_ERR_UNSUPPORTED;
-  return from_cuda(launch_verify(draft_probs, target_probs, tokens, seed,
-                                 offset, B, K, V, accepted_len, emitted_token,
-                                 sm_count(), stream));
+  return verify_rule(draft_probs, target_probs, tokens, seed, offset, B, K, V,
+                     accepted_len, emitted_token, false, stream);
+}
+
+dspark_status dspark_verify_block(const float* draft_probs,
+                                  const float* target_probs,
+                                  const int32_t* tokens, const uint64_t* seed,
+                                  const uint64_t* offset, int B, int K, int V,
+                                  int32_t* accepted_len, int32_t* emitted_token,
+                                  cudaStream_t stream) {
+  return verify_rule(draft_probs, target_probs, tokens, seed, offset, B, K, V,
+                     accepted_len, emitted_token, true, stream);
 }
 
 dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,

@@ -364,10 +364,12 @@ cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks, int buf,
 // Proposals of positions k_first .. k_first + k_count - 1.
 cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,
                              cudaStream_t stream);
+// block: the block-verification rule instead of the standard one.
 cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           const uint64_t* seed, const uint64_t* offset, int B,
                           int K, int V, int32_t* accepted_len,
-                          int32_t* emitted, int sms, cudaStream_t stream);
+                          int32_t* emitted, int sms, bool block,
+                          cudaStream_t stream);
 cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
                                int stream_id, int n, uint32_t* out,
                                float* gumbel, cudaStream_t stream);

@@ -101,13 +101,13 @@ __device__ __forceinline__ void load_block(const float* __restrict__ p,
 // the candidates, warp merge.  Warp-uniform control flow.
 __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
                                             float4 pv, float4 qv, bool resid,
-                                            const uint4& pre,
+                                            float wscale, const uint4& pre,
                                             const uint4 (&rk)[4]) {
   float wt[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
     const float pe = elem(pv, e);
-    const float d = resid ? __fsub_rn(pe, elem(qv, e)) : pe;
+    const float d = resid ? __fsub_rn(__fmul_rn(wscale, pe), elem(qv, e)) : pe;
     wt[e] = d > 0.0f ? d : 0.0f;  // NaN and non-positive weights: 0
     any |= wt[e] > 0.0f;
   }
@@ -140,15 +140,16 @@ __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
 }
 
 // Gumbel-max over log(weight) on this CTA's slice [lo, hi) of Philox blocks,
-// weights max(p - q, 0) when q != nullptr (the residual), else p; zero
-// weights never win.  (pre, rk): the folded Philox constants of noise
+// weights max(wscale p - q, 0) when q != nullptr (the residual; wscale is 1
+// for the standard rule, and 1 * p is p exactly), else p; zero weights never
+// win.  (pre, rk): the folded Philox constants of noise
 // stream 2 at the drawing position (philox_fold).  Then the cluster-wide winner and "some weight was
 // positive", identical in every CTA of the cluster.
 template <bool kVec>
 __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p,
                          const float* __restrict__ q, int V, int lo, int hi,
-                         const uint4& pre, const uint4 (&rk)[4], Best* part,
-                         int* any_part, Slot* slot) {
+                         float wscale, const uint4& pre, const uint4 (&rk)[4],
+                         Best* part, int* any_part, Slot* slot) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool resid = q != nullptr;
   Best st = {-INFINITY, kNoIndex};
@@ -160,9 +161,9 @@ __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p
     float4 p0, q0, p1, q1;
     load_block<kVec>(p, q, V, j0, hi, p0, q0);
     load_block<kVec>(p, q, V, j1, hi, p1, q1);
-    sweep_block(st, any, j0, p0, q0, resid, pre, rk);
+    sweep_block(st, any, j0, p0, q0, resid, wscale, pre, rk);
     if (base + kStride < hi)
-      sweep_block(st, any, j1, p1, q1, resid, pre, rk);
+      sweep_block(st, any, j1, p1, q1, resid, wscale, pre, rk);
   }
   any = __any_sync(0xffffffffu, any);
   if (lane == 0) {
@@ -193,7 +194,58 @@ __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p
   return all;
 }
 
+// Block verification's sums r_i = sum_x max(w_i p_i(x) - q_i(x), 0),
+// i = 1..K-1, over this CTA's slice of each row, then over the cluster.
+// Every CTA ends with the same values: each thread adds its blocks in
+// order, warps combine by a butterfly, the warps' sums and then the CTAs'
+// are added in a fixed order.
 template <bool kVec>
+__device__ void block_sums(cg::cluster_group& cluster, const float* __restrict__ q,
+                           const float* __restrict__ p, int b, int K, int V,
+                           int lo, int hi, const float* s_w, float* s_wpart,
+                           float* s_part, float* s_r) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int i = 1; i < K; ++i) {
+    const float* prow = p + ((size_t)b * (K + 1) + i) * V;
+    const float* qrow = q + ((size_t)b * K + i) * V;
+    const float wi = s_w[i];
+    float acc = 0.0f;
+    // four blocks in flight per thread
+    for (int j0 = lo + (int)threadIdx.x; j0 < hi; j0 += 4 * kVerifyThreads) {
+      float4 pv[4], qv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        load_block<kVec>(prow, qrow, V, j0 + u * kVerifyThreads, hi, pv[u], qv[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float t = __fsub_rn(__fmul_rn(wi, elem(pv[u], e)), elem(qv[u], e));
+          acc = __fadd_rn(acc, t > 0.0f ? t : 0.0f);  // NaN terms count as 0
+        }
+    }
+#pragma unroll
+    for (int mask = 16; mask > 0; mask >>= 1)
+      acc = __fadd_rn(acc, __shfl_xor_sync(0xffffffffu, acc, mask));
+    if (lane == 0) s_wpart[(i - 1) * kVerifyWarps + warp] = acc;
+  }
+  __syncthreads();
+  for (int i = 1 + (int)threadIdx.x; i < K; i += kVerifyThreads) {
+    float c = 0.0f;
+    for (int w = 0; w < kVerifyWarps; ++w) c = __fadd_rn(c, s_wpart[(i - 1) * kVerifyWarps + w]);
+    s_part[i - 1] = c;
+  }
+  cluster.sync();  // every CTA's partial sums are written
+  for (int i = 1 + (int)threadIdx.x; i < K; i += kVerifyThreads) {
+    float r = 0.0f;
+    for (unsigned c = 0; c < cluster.num_blocks(); ++c)
+      r = __fadd_rn(r, cluster.map_shared_rank(s_part, c)[i - 1]);
+    s_r[i] = r;
+  }
+  cluster.sync();  // every CTA has read them (and s_r is complete)
+}
+
+template <bool kVec, bool kBlock>
 __global__ void __launch_bounds__(kVerifyThreads, kVerifyMinBlocks)
 verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
               const int32_t* __restrict__ tokens, const uint64_t* seed,
@@ -205,6 +257,13 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
   __shared__ int any_part[kVerifyWarps];
   __shared__ Slot slot;
   __shared__ uint4 s_pre, s_rk[4];
+  // block rule: ratios, weights w_0..w_K, uniforms, sums r_1..r_{K-1}
+  __shared__ float s_ratio[kBlock ? DSPARK_MAX_K : 1];
+  __shared__ float s_w[kBlock ? DSPARK_MAX_K + 1 : 1];
+  __shared__ float s_eta[kBlock ? DSPARK_MAX_K : 1];
+  __shared__ float s_wpart[kBlock ? DSPARK_MAX_K * kVerifyWarps : 1];
+  __shared__ float s_part[kBlock ? DSPARK_MAX_K : 1];
+  __shared__ float s_r[kBlock ? DSPARK_MAX_K : 1];
   cg::cluster_group cluster = cg::this_cluster();
   const int C = (int)cluster.num_blocks();
   const int rank = (int)cluster.block_rank();
@@ -224,7 +283,12 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
     const float qd = q[((size_t)b * K + k) * V + d];
     const float pd = p[((size_t)b * (K + 1) + k) * V + d];
     const float u = accept_uniform(noise_block(sd, off, k, kNoiseAccept, 0u).x);
-    if (!(__fmul_rn(u, qd) < pd)) atomicMin(&s_first, k);
+    if (kBlock) {
+      s_ratio[k] = __fdiv_rn(pd, qd);
+      s_eta[k] = u;
+    } else if (!(__fmul_rn(u, qd) < pd)) {
+      atomicMin(&s_first, k);
+    }
   }
   __syncthreads();
   if (s_bad) {  // the same in every CTA of the cluster: all return here
@@ -234,6 +298,41 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
     }
     return;
   }
+  // this CTA's slice of the row's Philox blocks
+  const int n_blk = (V + 3) / 4;
+  const int per = (n_blk + C - 1) / C;
+  const int lo = min(rank * per, n_blk), hi = min(lo + per, n_blk);
+  float wscale = 1.0f;
+  if (kBlock) {
+    if (threadIdx.x == 0) {  // w_{k+1} = min(w_k (p/q), 1); NaN counts as 0
+      float w = 1.0f;
+      s_w[0] = w;
+      for (int k = 0; k < K; ++k) {
+        const float t = __fmul_rn(w, s_ratio[k]);
+        w = t < 1.0f ? t : (t >= 1.0f ? 1.0f : 0.0f);
+        s_w[k + 1] = w;
+      }
+    }
+    __syncthreads();
+    block_sums<kVec>(cluster, q, p, b, K, V, lo, hi, s_w, s_wpart, s_part, s_r);
+    if (threadIdx.x == 0) {  // the longest prefix whose uniform is under h_i
+      int tau = 0;
+      for (int i = 1; i <= K; ++i) {
+        float h;
+        if (i < K) {
+          const float r = s_r[i];
+          const float den = __fadd_rn(r, __fsub_rn(1.0f, s_w[i]));
+          h = den > 0.0f ? __fdiv_rn(r, den) : 1.0f;
+        } else {
+          h = s_w[K];
+        }
+        if (s_eta[i - 1] <= h) tau = i;
+      }
+      s_first = tau;
+    }
+    __syncthreads();
+    wscale = s_w[s_first];
+  }
   const int kk = s_first;
   if (threadIdx.x == 0)
     philox_fold(s_pre, s_rk, (uint32_t)sd, (uint32_t)(sd >> 32),
@@ -242,15 +341,11 @@ verify_kernel(const float* __restrict__ q, const float* __restrict__ p,
   __syncthreads();
   const float* prow = p + ((size_t)b * (K + 1) + kk) * V;
   const float* qrow = kk < K ? q + ((size_t)b * K + kk) * V : nullptr;
-  // this CTA's slice of the row's Philox blocks
-  const int n_blk = (V + 3) / 4;
-  const int per = (n_blk + C - 1) / C;
-  const int lo = min(rank * per, n_blk), hi = min(lo + per, n_blk);
-  Slot r = draw_row<kVec>(cluster, prow, qrow, V, lo, hi, s_pre, s_rk, part,
-                          any_part, &slot);
+  Slot r = draw_row<kVec>(cluster, prow, qrow, V, lo, hi, wscale, s_pre, s_rk,
+                          part, any_part, &slot);
   if (qrow != nullptr && !r.any)  // residual all zero: draw from p itself
-    r = draw_row<kVec>(cluster, prow, nullptr, V, lo, hi, s_pre, s_rk, part,
-                       any_part, &slot);
+    r = draw_row<kVec>(cluster, prow, nullptr, V, lo, hi, 1.0f, s_pre, s_rk,
+                       part, any_part, &slot);
   if (rank == 0 && threadIdx.x == 0) {
     accepted_len[b] = kk;
     emitted[b] = r.idx == kNoIndex ? 0 : r.idx;
@@ -269,7 +364,7 @@ int verify_cluster_size(int B, int V, int sms) {
   return c < 1 ? 1 : c;
 }
 
-template <bool kVec>
+template <bool kVec, bool kBlock>
 cudaError_t launch_verify_t(const float* q, const float* p,
                             const int32_t* tokens, const uint64_t* seed,
                             const uint64_t* offset, int B, int K, int V,
@@ -287,8 +382,8 @@ cudaError_t launch_verify_t(const float* q, const float* p,
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, verify_kernel<kVec>, q, p, tokens, seed,
-                            offset, K, V, accepted_len, emitted);
+  return cudaLaunchKernelEx(&cfg, verify_kernel<kVec, kBlock>, q, p, tokens,
+                            seed, offset, K, V, accepted_len, emitted);
 }
 
 }  // namespace
@@ -296,13 +391,19 @@ cudaError_t launch_verify_t(const float* q, const float* p,
 cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           const uint64_t* seed, const uint64_t* offset, int B,
                           int K, int V, int32_t* accepted_len,
-                          int32_t* emitted, int sms, cudaStream_t stream) {
+                          int32_t* emitted, int sms, bool block,
+                          cudaStream_t stream) {
   const int C = verify_cluster_size(B, V, sms);
-  if (V % 4 == 0)
-    return launch_verify_t<true>(q, p, tokens, seed, offset, B, K, V,
-                                 accepted_len, emitted, C, stream);
-  return launch_verify_t<false>(q, p, tokens, seed, offset, B, K, V,
-                                accepted_len, emitted, C, stream);
+  const bool vec = V % 4 == 0;
+  if (block)
+    return vec ? launch_verify_t<true, true>(q, p, tokens, seed, offset, B, K, V,
+                                             accepted_len, emitted, C, stream)
+               : launch_verify_t<false, true>(q, p, tokens, seed, offset, B, K, V,
+                                              accepted_len, emitted, C, stream);
+  return vec ? launch_verify_t<true, false>(q, p, tokens, seed, offset, B, K, V,
+                                            accepted_len, emitted, C, stream)
+             : launch_verify_t<false, false>(q, p, tokens, seed, offset, B, K, V,
+                                             accepted_len, emitted, C, stream);
 }
 
 }  // namespace dspark

@@ -411,24 +411,33 @@ def run_ours(args, rank, world):
     del tl
     acc_len = torch.empty(B, dtype=torch.int32, device="cuda")
     emitted = torch.empty(B, dtype=torch.int32, device="cuda")
-    for _ in range(3):
-        pkg.verify_standard(probs, target, tokens, dev["seed"], dev["offset"],
-                            accepted_len=acc_len, emitted_token=emitted)
-    torch.cuda.synchronize()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    n_ver = 20
-    f0.record(cur)
-    for _ in range(n_ver):
-        pkg.verify_standard(probs, target, tokens, dev["seed"], dev["offset"],
-                            accepted_len=acc_len, emitted_token=emitted)
-    f1.record(cur)
-    torch.cuda.synchronize()
-    verify_us = f0.elapsed_time(f1) / n_ver * 1e3
+
+    def time_rule(fn, n_ver=20):
+        for _ in range(3):
+            fn(probs, target, tokens, dev["seed"], dev["offset"],
+               accepted_len=acc_len, emitted_token=emitted)
+        torch.cuda.synchronize()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        f0.record(cur)
+        for _ in range(n_ver):
+            fn(probs, target, tokens, dev["seed"], dev["offset"],
+               accepted_len=acc_len, emitted_token=emitted)
+        f1.record(cur)
+        torch.cuda.synchronize()
+        return f0.elapsed_time(f1) / n_ver * 1e3, float(acc_len.float().mean().item())
+
+    verify_us, mean_std = time_rule(pkg.verify_standard)
+    block_us, mean_blk = time_rule(pkg.verify_block)
     verify = {"us_per_call": verify_us, "B": B, "K": K, "V": V,
-              "mean_accepted_len": float(acc_len.float().mean().item()),
+              "mean_accepted_len": mean_std,
               "upper_bound_bytes": B * V * 8,
               "note": "standard rejection verification of the benchmark "
-                      "block's drafts (one thread-block cluster of CTAs per request)"}
+                      "block's drafts (one thread-block cluster of CTAs per request)",
+              "block": {"us_per_call": block_us, "mean_accepted_len": mean_blk,
+                        "bytes": 2 * B * (K - 1) * V * 4 + B * V * 8,
+                        "note": "block verification of the same drafts: reads "
+                                "the K-1 rows p_1..p_{K-1}, q_1..q_{K-1} in full"}}
     del target
 
     if rank == 0:

@@ -255,6 +255,34 @@ DSPARK_API dspark_status dspark_verify_standard(const float* draft_probs,
                                      cudaStream_t stream);
 
 /*
+ * dspark_verify_block -- block verification of the drafts (PR #21, "2.
+ * Golden sampling semantics": the block value of rejection_sample_method,
+ * the block verification of Sun et al., 2024), for B requests.  Arguments,
+ * layouts, outputs and errors are those of dspark_verify_standard.
+ * With d_k = tokens[b,k], q_k = draft_probs[b,k], p_k = target_probs[b,k]:
+ *   w_0 = 1, w_{k+1} = min(w_k * (p_k[d_k] / q_k[d_k]), 1) in float32
+ *   (a NaN weight counts as 0);
+ *   h_i = r_i / (r_i + 1 - w_i) for i = 1..K-1, with
+ *   r_i = sum_x max(w_i p_i(x) - q_i(x), 0) (1 when r_i = 1 - w_i = 0);
+ *   h_K = w_K;
+ *   accepted_len = the largest i in 1..K with u_{i-1} <= h_i (0 if none),
+ *   u_k the uniform of the standard rule;
+ *   emitted_token: Gumbel-max with stream 2 noise at position accepted_len
+ *   over p_K when accepted_len = K, else over max(w p - q, 0) at that
+ *   position (over p itself if that is all zero).
+ * The sums r_i run in float32 in a fixed order (results are reproducible
+ * call to call).  The call reads the K-1 rows p_1..p_{K-1} and q_1..q_{K-1}
+ * in full.  On average it accepts at least as many drafts as the standard
+ * rule, and it is lossless.
+ */
+DSPARK_API dspark_status dspark_verify_block(const float* draft_probs,
+                                  const float* target_probs,
+                                  const int32_t* tokens, const uint64_t* seed,
+                                  const uint64_t* offset, int B, int K, int V,
+                                  int32_t* accepted_len, int32_t* emitted_token,
+                                  cudaStream_t stream);
+
+/*
  * dspark_noise_words -- diagnostic: writes the n raw Philox words the
  * sampler uses for elements 0..n-1 of (seed, offset, position k, stream),
  * i.e. out[v] = word (v & 3) of Philox4x32-10(counter (v >> 2,
