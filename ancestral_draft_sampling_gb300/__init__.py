@@ -15,7 +15,8 @@ from typing import Optional
 from . import _lib
 from ._lib import BF16, F32, DsparkError  # noqa: F401
 
-__all__ = ["draft_block", "draft_block_noalloc", "draft_block_profile",
+__all__ = ["draft_block", "draft_block_per_request", "draft_block_noalloc",
+           "draft_block_profile",
            "draft_block_host", "HostWorkspace", "verify_standard", "verify_block",
            "noise_words", "workspace_bytes", "read_device_error",
            "DraftWorkspace", "DsparkError", "F32", "BF16", "version"]
@@ -104,6 +105,56 @@ def draft_block(base_logits, U, Wb, d0, seed, offset, T: float, *,
         _ptr(draft_probs), _ptr(workspace.buffer), workspace.nbytes,
         _stream(stream))
     _lib.check("dspark_draft_block", st)
+    return tokens, logits, draft_probs
+
+
+def draft_block_per_request(base_logits, U, Wb, d0, seed, offset, temperature, *,
+                            greedy=None, pad_row=None, tokens=None, logits=None,
+                            draft_probs=None, slot=None,
+                            workspace: Optional[DraftWorkspace] = None,
+                            stream=None):
+    """draft_block with temperature [B] float32 (device) per request and,
+    when slot [B] int32 is given, proposals written to draft_probs[slot[b]]
+    (draft_probs [num_slots, K, V], which must then be passed in).  Returns
+    (tokens, logits, draft_probs).  See include/dspark.h."""
+    torch = _torch()
+    B, K, V = base_logits.shape
+    r = U.shape[1]
+    if tuple(U.shape) != (V, r) or tuple(Wb.shape) != (r, V):
+        raise ValueError("U must be [V, r] and Wb [r, V]")
+    if U.dtype != Wb.dtype:
+        raise TypeError("U and Wb must share a dtype")
+    if temperature.dtype != torch.float32 or tuple(temperature.shape) != (B,):
+        raise TypeError("temperature must be float32 [B]")
+    for t in (base_logits, U, Wb, d0, seed, offset, greedy, pad_row, temperature,
+              slot):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    dev = base_logits.device
+    if slot is not None:
+        if slot.dtype != torch.int32 or tuple(slot.shape) != (B,):
+            raise TypeError("slot must be int32 [B]")
+        if draft_probs is None or draft_probs.dim() != 3 or \
+                tuple(draft_probs.shape[1:]) != (K, V):
+            raise ValueError("with slot, pass draft_probs [num_slots, K, V]")
+        num_slots = draft_probs.shape[0]
+    else:
+        num_slots = 0
+    if tokens is None:
+        tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if logits is None:
+        logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if draft_probs is None:
+        draft_probs = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = DraftWorkspace(B, K, V, r, device=dev)
+    st = _lib.load().dspark_draft_block_per_request(
+        _ptr(base_logits), _dtype_code(base_logits), _ptr(U), _ptr(Wb),
+        _dtype_code(U), _ptr(d0), _ptr(seed), _ptr(offset), _ptr(temperature),
+        _ptr(greedy), _ptr(pad_row), B, K, V, r, _ptr(tokens), _ptr(logits),
+        _ptr(draft_probs), _ptr(slot), num_slots, _ptr(workspace.buffer),
+        workspace.nbytes, _stream(stream))
+    _lib.check("dspark_draft_block_per_request", st)
     return tokens, logits, draft_probs
 
 

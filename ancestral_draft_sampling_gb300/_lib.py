@@ -27,6 +27,7 @@ STATUS = {
 # Every symbol include/dspark.h declares.
 EXPORTED = (
     "dspark_draft_workspace_bytes",
+    "dspark_draft_block_per_request",
     "dspark_draft_block",
     "dspark_draft_block_profile",
     "dspark_draft_block_noalloc",
@@ -87,6 +88,10 @@ def load() -> ctypes.CDLL:
         lib.dspark_verify_standard.restype = I
         lib.dspark_verify_block.argtypes = [P, P, P, P, P, I, I, I, P, P, P]
         lib.dspark_verify_block.restype = I
+        lib.dspark_draft_block_per_request.argtypes = [
+            P, I, P, P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, I, P,
+            ctypes.c_size_t, P]
+        lib.dspark_draft_block_per_request.restype = I
         lib.dspark_noise_words.argtypes = [U64, U64, I, I, I, P, P, P]
         lib.dspark_noise_words.restype = I
         lib.dspark_read_device_error.argtypes = [P, P, P]

@@ -349,6 +349,32 @@ dspark_status dspark_draft_block(
   return run_block(a, stream, nullptr);
 }
 
+dspark_status dspark_draft_block_per_request(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, const float* temperature,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, const int32_t* slot,
+    int num_slots, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream) {
+  if (!temperature || (reinterpret_cast<uintptr_t>(temperature) & 3u) != 0)
+    return DSPARK_ERR_INVALID_ARG;
+  if (slot && ((reinterpret_cast<uintptr_t>(slot) & 3u) != 0 || num_slots <= 0 ||
+               num_slots > 65535 * 16))
+    return DSPARK_ERR_INVALID_ARG;
+  DraftArgs a{};
+  // T = 2 only passes the scalar check; every kernel reads temperature[b]
+  dspark_status st = prepare_draft(
+      base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, 2.0f, greedy,
+      pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
+      workspace_bytes, a);
+  if (st != DSPARK_OK) return st;
+  a.temperature = temperature;
+  a.slot = slot;
+  a.num_slots = slot ? num_slots : 0;
+  return run_block(a, stream, nullptr);
+}
+
 dspark_status dspark_draft_block_profile(
     const void* base_logits, dspark_dtype base_dtype, const void* U,
     const void* Wb, dspark_dtype w_dtype, const int32_t* d0,

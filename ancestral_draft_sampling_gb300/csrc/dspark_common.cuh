@@ -322,6 +322,8 @@ enum DeviceError : int {
   kDevErrNone = 0,
   kDevErrBadToken = 1,  // a d0 entry outside [0, V) (token 0 used instead)
   kDevErrTimeout = 2,   // a bounded wait inside a kernel ran out
+  kDevErrBadTemperature = 3,  // a per-request temperature not finite and > 0
+  kDevErrBadSlot = 4,   // a proposal slot outside [0, num_slots)
 };
 
 // ------------------------------------------------------- kernel launchers
@@ -344,8 +346,23 @@ struct DraftArgs {
   ChunkStat* stats;
   float* rowstats;
   unsigned long long* hints;  // [B] x kHintRowKeys; keys 0..K-1 zeroed per block
+  // per-request entry point: temperature [B] (device) replaces T; request
+  // b's proposals go to draft_probs slot slot[b] of num_slots (both null /
+  // 0 otherwise)
+  const float* temperature;
+  const int32_t* slot;
+  int num_slots;
   int* control;
 };
+
+// The temperature of request b: its own when the call gives per-request
+// temperatures (a value that is not finite and positive counts as 1), else
+// the block's T.
+__device__ __forceinline__ float request_temperature(const DraftArgs& a, int b) {
+  if (a.temperature == nullptr) return a.T;
+  const float t = a.temperature[b];
+  return (t > 0.0f && t <= 3.40282347e38f) ? t : 1.0f;
+}
 
 // Launch helpers (each returns the cudaGetLastError of its launch).
 cudaError_t launch_position_generic(const DraftArgs& a, int k, int n_chunks,

@@ -69,8 +69,22 @@ proposals_kernel(DraftArgs a, int k_first, int k_count) {
   const bool greedy = a.greedy != nullptr && a.greedy[b] != 0;
   const int token = greedy ? a.tokens[row] : -1;
   const float* __restrict__ lrow = a.logits + (size_t)row * V;
-  float* __restrict__ qrow = a.probs + (size_t)row * V;
-  const float T = a.T;
+  // per-request entry point: request b's proposals go to slot slot[b]
+  const int k = row - b * a.K;
+  int dst = b;
+  if (a.slot != nullptr) {
+    dst = a.slot[b];
+    if (dst < 0 || dst >= a.num_slots) {  // nothing is written for it
+      if (k == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        a.control[0] = kDevErrBadSlot;
+      return;
+    }
+  }
+  float* __restrict__ qrow = a.probs + ((size_t)dst * a.K + k) * V;
+  const float T = request_temperature(a, b);
+  if (a.temperature != nullptr && k == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
+      T == 1.0f && a.temperature[b] != 1.0f)  // not finite and positive
+    a.control[0] = kDevErrBadTemperature;
   const int seg = kPropThreads * kPropPerThread;
   const int v_begin = blockIdx.y * seg;
   if (kVec) {

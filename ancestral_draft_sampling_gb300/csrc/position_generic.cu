@@ -217,10 +217,11 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
         float base4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (!pad) load_base4<BT, kVec>(base + row * V, v, V, base4);
         float l[4], s[4], score[4];
+        const float T = request_temperature(a, b);
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           l[e] = pad ? acc[q][e] : __fadd_rn(base4[e], acc[q][e]);
-          s[e] = scale(l[e], a.T);
+          s[e] = scale(l[e], T);
         }
         store_logits4<kVec>(a.logits + row * V, v, V, l);
         if (greedy) {

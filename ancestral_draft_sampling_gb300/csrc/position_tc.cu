@@ -101,7 +101,8 @@ struct alignas(16) RowConst {
   uint4 pre;     // rounds 1-2 folded: (C1, D2, E2, F2), see row_noise
   uint4 rk[4];   // round keys of rounds 3..10: rk[j] = rounds 2j+3, 2j+4
   uint32_t flags;  // bit 0: padding row, bit 1: greedy request
-  uint32_t pad[3];
+  float T;         // the request's temperature (per-request entry point)
+  uint32_t pad[2];
 };
 constexpr uint32_t kRowPad = 1u, kRowGreedy = 2u;
 
@@ -398,7 +399,9 @@ __device__ __forceinline__ void scaled4(const float4 l4, float T,
   s[3] = scale<kUnitT>(l4.w, T);
 }
 
-template <typename BT, bool kUnitT>
+// kRowT: per-request temperatures (the per-request entry point); each row
+// divides by its own T, rows whose T is 1 skip the division.
+template <typename BT, bool kUnitT, bool kRowT>
 __global__ void __launch_bounds__(kThreads, 1)
 position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
                    const __grid_constant__ CUtensorMap base_map,
@@ -477,7 +480,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       RowConst rc;
       uint32_t k0 = 0, k1 = 0, c2 = 0, c3 = 0;
       rc.flags = 0;
-      rc.pad[0] = rc.pad[1] = rc.pad[2] = 0;
+      rc.T = 1.0f;
+      rc.pad[0] = rc.pad[1] = 0;
       if (b < a.B) {
         k0 = (uint32_t)a.seed[b];
         k1 = (uint32_t)(a.seed[b] >> 32);
@@ -485,6 +489,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         c3 = (uint32_t)(a.offset[b] >> 32);
         rc.flags = (a.pad_row != nullptr && a.pad_row[b] != 0 ? kRowPad : 0u) |
                    (a.greedy != nullptr && a.greedy[b] != 0 ? kRowGreedy : 0u);
+        if (kRowT) rc.T = request_temperature(a, b);
       }
       row_constants(rc, k0, k1, (uint32_t)P.k | ((uint32_t)kNoiseDraft << 16),
                     c2, c3);
@@ -829,7 +834,15 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
             const uint4 w = wn[i - i0];
             const float4 l4 = *reinterpret_cast<const float4*>(tile + b * kTileV + 4 * lane);
             float sv[4];
-            scaled4<kUnitT>(l4, T, sv);
+            if (!kRowT) {
+              scaled4<kUnitT>(l4, T, sv);
+            } else {
+              const float Tb = rows[b].T;
+              if (Tb == 1.0f)
+                scaled4<true>(l4, Tb, sv);
+              else
+                scaled4<false>(l4, Tb, sv);
+            }
             const uint32_t h = (uint32_t)(__shfl_sync(0xffffffffu, hint_in, i) >> 32);
             const float4 q = rstate[i];
             RowState st{sums[i], q.x, q.y, q.z, __float_as_int(q.w)};  // ref, sref, h, idx
@@ -973,12 +986,12 @@ CUresult encode_position_map(CUtensorMap* map, CUtensorMapDataType dt,
 // serialisation behind the previous position's pick kernel: their set-up
 // and first Wb / drafter-logit loads overlap the end of the previous
 // position; they wait for its token before the gather.
-template <typename BT, bool kUnitT>
+template <typename BT, bool kUnitT, bool kRowT>
 cudaError_t launch_typed(const CUtensorMap& wb, const CUtensorMap& bm,
                          const CUtensorMap& om, const TcParams& P, size_t smem,
                          int n_chunks, bool overlap_previous,
                          cudaStream_t stream) {
-  auto kern = position_tc_kernel<BT, kUnitT>;
+  auto kern = position_tc_kernel<BT, kUnitT, kRowT>;
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
@@ -1052,11 +1065,17 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
   P.bar_off = L.bar_off;
   const bool unit = a.T == 1.0f;
   const bool pdl = k > 0;
+  if (a.temperature != nullptr)
+    return elt == 4
+               ? launch_typed<float, false, true>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
+               : launch_typed<uint16_t, false, true>(wb, bm, om, P, L.smem, n_chunks, pdl,
+                                                     stream);
   if (elt == 4)
-    return unit ? launch_typed<float, true>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
-                : launch_typed<float, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream);
-  return unit ? launch_typed<uint16_t, true>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
-              : launch_typed<uint16_t, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream);
+    return unit ? launch_typed<float, true, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
+                : launch_typed<float, false, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream);
+  return unit ? launch_typed<uint16_t, true, false>(wb, bm, om, P, L.smem, n_chunks, pdl, stream)
+              : launch_typed<uint16_t, false, false>(wb, bm, om, P, L.smem, n_chunks, pdl,
+                                                     stream);
 }
 
 }  // namespace dspark

@@ -147,6 +147,39 @@ DSPARK_API dspark_status dspark_draft_block_profile(
     cudaStream_t stream);
 
 /*
+ * dspark_draft_block_per_request -- dspark_draft_block with a temperature
+ * per request and slot-indexed proposals, as a serving batch needs them
+ * (PR #27, "2. One fused kernel per draft position": the proposal writer
+ * stores q_k into the slot-indexed draft_probs; the temperature of a draft
+ * is its request's sampling temperature).
+ *
+ *   temperature  [B] float32, device, 4-byte aligned: request b's T.  A
+ *                value that is not finite and positive counts as 1 and sets
+ *                the device error word to 3 (DSPARK_ERR_DEVICE via
+ *                dspark_read_device_error).
+ *   draft_probs  [num_slots, K, V] float32 when slot is given, else [B,K,V].
+ *   slot         [B] int32 device (4-byte aligned) or NULL: request b's
+ *                proposals are written to draft_probs[slot[b]]; slots of
+ *                different requests must differ; a slot outside
+ *                [0, num_slots) writes nothing for that request and sets the
+ *                device error word to 4.  Slots of no request are left as
+ *                they are.
+ *   num_slots    rows of draft_probs (ignored when slot is NULL).
+ * Every other argument, the workspace (dspark_draft_workspace_bytes) and the
+ * errors are those of dspark_draft_block; tokens and logits stay [B,K] and
+ * [B,K,V].  With equal temperatures T the outputs are bitwise those of
+ * dspark_draft_block with T.
+ */
+DSPARK_API dspark_status dspark_draft_block_per_request(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, const float* temperature,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, const int32_t* slot,
+    int num_slots, void* workspace, size_t workspace_bytes,
+    cudaStream_t stream);
+
+/*
  * dspark_draft_block_noalloc -- dspark_draft_block for callers that cannot
  * allocate device memory: code that is handed only its input and output
  * buffers by a host runtime that owns all device memory (an inference

@@ -164,9 +164,34 @@ class BlockResult:
     __slots__ = ("tokens", "logits", "probs", "rowstats", "top2")
 
 
+def request_temperatures(T, B):
+    """Per-request temperatures from a scalar or a [B] array; a value that is
+    not finite and positive counts as 1 (the per-request entry point's
+    reading)."""
+    if np.ndim(T) == 0:
+        return np.full(B, float(T), dtype=np.float32)
+    t = np.asarray(T, dtype=np.float32).copy()
+    t[~(np.isfinite(t) & (t > 0))] = 1.0
+    return t
+
+
 def draft_block(base, U, Wb, d0, seed, offset, T, greedy=None,
                 pad_row=None) -> BlockResult:
-    """The whole ancestral block, row after row (single thread)."""
+    """The whole ancestral block, row after row (single thread).  T is a
+    scalar, or a [B] array of per-request temperatures (then each request
+    runs as its own block with its own T)."""
+    if np.ndim(T) > 0:
+        B = base.shape[0]
+        Ts = request_temperatures(T, B)
+        parts = [draft_block(base[b:b + 1], U, Wb, d0[b:b + 1], seed[b:b + 1],
+                             offset[b:b + 1], float(Ts[b]),
+                             None if greedy is None else greedy[b:b + 1],
+                             None if pad_row is None else pad_row[b:b + 1])
+                 for b in range(B)]
+        out = BlockResult()
+        for name in BlockResult.__slots__:
+            setattr(out, name, np.concatenate([getattr(x, name) for x in parts]))
+        return out
     lib = _load()
     B, K, V = base.shape
     r = U.shape[1]
@@ -204,6 +229,7 @@ def draft_chains(base, U, Wb, d0, seed, offset, T, depth, greedy=None,
     releases the GIL).  Returns {b: [PositionResult per position]}."""
     todo = [b for b in range(len(depth)) if depth[b] > 0]
     threads = threads or max(1, min(len(todo), os.cpu_count() or 1))
+    Ts = request_temperatures(T, len(depth))  # T: scalar or per request
 
     def one(b):
         is_pad = bool(pad_row[b]) if pad_row is not None else False
@@ -212,8 +238,8 @@ def draft_chains(base, U, Wb, d0, seed, offset, T, depth, greedy=None,
         for k in range(int(depth[b])):
             row = None if is_pad else base[b, k]
             res = draft_position(row, U, Wb, prev, int(seed[b]),
-                                 int(offset[b]), k, T, greedy=is_greedy,
-                                 is_pad=is_pad)
+                                 int(offset[b]), k, float(Ts[b]),
+                                 greedy=is_greedy, is_pad=is_pad)
             chain.append(res)
             prev = res.token
         return chain

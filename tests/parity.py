@@ -93,6 +93,7 @@ def check_block_against_oracle(w, tokens, logits, probs, rows=None,
     chains = oracle.draft_chains(w.base, w.U, w.Wb, w.d0, w.seed, w.offset,
                                  w.T, depth, greedy=w.greedy,
                                  pad_row=w.pad_row, threads=threads)
+    Ts = oracle.request_temperatures(w.T, B)  # w.T: scalar or per request
     # first position whose token differs from the oracle's draw, per request
     diverged = {}
     for b, chain in chains.items():
@@ -123,7 +124,7 @@ def check_block_against_oracle(w, tokens, logits, probs, rows=None,
         else:
             np.testing.assert_allclose(
                 probs[b, k], o.probs, atol=PROB_ATOL,
-                rtol=prob_rtol(o.logits, w.T), equal_nan=True,
+                rtol=prob_rtol(o.logits, float(Ts[b])), equal_nan=True,
                 err_msg=f"draft_probs {where}")
         checked += 1
     return {"rows": checked, "near_tie_token_diffs": len(diverged),
