@@ -16,7 +16,10 @@ of Gumbel-max against the closed-form softmax, conditioning, the greedy chain
 against numpy's argmax, the bias against a float64 GEMV, proposal sums, and
 losslessness of standard verification) and ``tests/test_oracle_block.py``
 (block verification: losslessness by chi-square, its reduction to the
-standard rule at K = 1, identical draft and target).
+standard rule at K = 1, identical draft and target) and
+``tests/test_oracle_sampler.py`` (temperature-only sampling: chi-square
+against the closed-form softmax, the draft positions' softmax, greedy rows,
+independent noise streams).
 """
 from __future__ import annotations
 
@@ -81,6 +84,9 @@ def _load():
         lib.oracle_verify_block.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P,
                                             P, P]
         lib.oracle_verify_block.restype = I
+        lib.oracle_sample_temperature.argtypes = [P, P, P, P, P, P, I, I, P, P,
+                                                  P, P, P]
+        lib.oracle_sample_temperature.restype = I
         _lib = lib
         return lib
 
@@ -304,4 +310,37 @@ def verify_block(draft_probs, target_probs, tokens, seed, offset) -> VerifyResul
                                  _ptr(out.h), _ptr(out.eta), _ptr(scratch))
     if rc != 0:
         raise ValueError("oracle_verify_block rejected its arguments")
+    return out
+
+
+class SampleResult:
+    __slots__ = ("tokens", "probs", "rowstats", "top2")
+
+
+def sample_temperature(logits, T, seed, offset, greedy=None,
+                       position=None) -> SampleResult:
+    """Temperature-only target sampling (PR #27, "1. Temperature-only
+    sampling runs no filter"), see oracle_sample_temperature.  logits [R,V]
+    float32; T scalar or [R] (an invalid value counts as 1, the reading of
+    the per-request entry points)."""
+    lib = _load()
+    R, V = logits.shape
+    x = np.ascontiguousarray(logits, dtype=np.float32)
+    t = request_temperatures(T, R)
+    s = np.ascontiguousarray(seed, dtype=np.uint64)
+    o = np.ascontiguousarray(offset, dtype=np.uint64)
+    g = None if greedy is None else np.ascontiguousarray(greedy, dtype=np.uint8)
+    pos = None if position is None else np.ascontiguousarray(position, dtype=np.int32)
+    out = SampleResult()
+    out.tokens = np.zeros(R, dtype=np.int32)
+    out.probs = np.empty((R, V), dtype=np.float64)
+    out.rowstats = np.empty((R, 2), dtype=np.float64)
+    out.top2 = np.empty((R, 2), dtype=np.float32)
+    scratch = np.empty(V, dtype=np.float64)
+    rc = lib.oracle_sample_temperature(
+        _ptr(x), _ptr(t), _ptr(g), _ptr(s), _ptr(o), _ptr(pos), R, V,
+        _ptr(out.tokens), _ptr(out.probs), _ptr(out.rowstats), _ptr(out.top2),
+        _ptr(scratch))
+    if rc != 0:
+        raise ValueError("oracle_sample_temperature rejected its arguments")
     return out

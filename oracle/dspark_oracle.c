@@ -130,6 +130,70 @@ static double load_elem(const void* p, int dtype, size_t i) {
 
 /* ---------------------------------------------------- one draft position */
 
+/* The decision and the proposal of one row from its float32 logits: the
+ * argmax of s = l / T (greedy) or of float(s + g) with g the Gumbel variate
+ * of noise `stream` at position k (sampled), lowest index on ties, NaN and
+ * -inf never winning; and q = softmax(s) in double (one-hot for greedy).
+ * Shared by the draft positions (stream 0) and the temperature-only target
+ * sampler (stream 3). */
+static void oracle_sample_row(const float* logits, int V, uint64_t seed,
+                              uint64_t offset, int k, int stream, float T,
+                              int greedy, double* probs_out, int* token_out,
+                              double* M_out, double* S_out, float* best_out,
+                              float* second_out) {
+  /* decision: argmax of s (greedy) or of float(s + g) (sampled) */
+  int token = 0;
+  float best = -INFINITY;
+  int found = 0;
+  for (int v = 0; v < V; ++v) {
+    float s = logits[v] / T;
+    float score;
+    if (greedy) {
+      score = s;
+    } else {
+      float g = (float)oracle_gumbel(oracle_noise_word(seed, offset, k, stream,
+                                                       (uint32_t)v));
+      score = s + g;
+    }
+    if (score > best) { /* NaN and -inf never win; ties keep the lower v */
+      best = score;
+      token = v;
+      found = 1;
+    }
+  }
+  float second = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    if (v == token) continue;
+    float s = logits[v] / T;
+    float score = s;
+    if (!greedy)
+      score = s + (float)oracle_gumbel(
+                      oracle_noise_word(seed, offset, k, stream, (uint32_t)v));
+    if (!isnan(score) && score > second) second = score;
+  }
+
+  /* proposal q = softmax(s) in double from the float32 s */
+  double M = -INFINITY;
+  for (int v = 0; v < V; ++v) {
+    double s = (double)(logits[v] / T);
+    if (!isnan(s) && s > M) M = s;
+  }
+  double S = 0.0;
+  for (int v = 0; v < V; ++v) S += exp((double)(logits[v] / T) - M);
+  if (greedy) {
+    for (int v = 0; v < V; ++v) probs_out[v] = (v == token) ? 1.0 : 0.0;
+  } else {
+    for (int v = 0; v < V; ++v)
+      probs_out[v] = exp((double)(logits[v] / T) - M) / S;
+  }
+
+  *token_out = token;
+  *M_out = M;
+  *S_out = S;
+  *best_out = found ? best : -INFINITY;
+  *second_out = second;
+}
+
 /*
  * One draft position of one request.
  *
@@ -171,57 +235,8 @@ int oracle_draft_position(const void* base_row, int base_dtype, int is_pad,
     logits_out[v] = (float)(base + bias_scratch[v]);
   }
 
-  /* decision: argmax of s (greedy) or of float(s + g) (sampled) */
-  int token = 0;
-  float best = -INFINITY;
-  int found = 0;
-  for (int v = 0; v < V; ++v) {
-    float s = logits_out[v] / T;
-    float score;
-    if (greedy) {
-      score = s;
-    } else {
-      float g = (float)oracle_gumbel(oracle_noise_word(seed, offset, k, 0,
-                                                       (uint32_t)v));
-      score = s + g;
-    }
-    if (score > best) { /* NaN and -inf never win; ties keep the lower v */
-      best = score;
-      token = v;
-      found = 1;
-    }
-  }
-  float second = -INFINITY;
-  for (int v = 0; v < V; ++v) {
-    if (v == token) continue;
-    float s = logits_out[v] / T;
-    float score = s;
-    if (!greedy)
-      score = s + (float)oracle_gumbel(
-                      oracle_noise_word(seed, offset, k, 0, (uint32_t)v));
-    if (!isnan(score) && score > second) second = score;
-  }
-
-  /* proposal q = softmax(s) in double from the float32 s */
-  double M = -INFINITY;
-  for (int v = 0; v < V; ++v) {
-    double s = (double)(logits_out[v] / T);
-    if (!isnan(s) && s > M) M = s;
-  }
-  double S = 0.0;
-  for (int v = 0; v < V; ++v) S += exp((double)(logits_out[v] / T) - M);
-  if (greedy) {
-    for (int v = 0; v < V; ++v) probs_out[v] = (v == token) ? 1.0 : 0.0;
-  } else {
-    for (int v = 0; v < V; ++v)
-      probs_out[v] = exp((double)(logits_out[v] / T) - M) / S;
-  }
-
-  *token_out = token;
-  *M_out = M;
-  *S_out = S;
-  *best_out = found ? best : -INFINITY;
-  *second_out = second;
+  oracle_sample_row(logits_out, V, seed, offset, k, 0, T, greedy, probs_out,
+                    token_out, M_out, S_out, best_out, second_out);
   return 0;
 }
 
@@ -453,6 +468,52 @@ int oracle_verify_block(const float* draft_probs, const float* target_probs,
     if (emit_top2) {
       emit_top2[2 * b] = best;
       emit_top2[2 * b + 1] = second;
+    }
+  }
+  return 0;
+}
+
+/* ------------------------------------------ temperature-only target sampler */
+
+/*
+ * Temperature-only sampling of target rows: PR #27, "1. Temperature-only
+ * sampling runs no filter" (softmax and sampling only, no top-k, top-p or
+ * min-p).  Row i of logits [R,V] (float32) is drawn like a draft position
+ * (oracle_sample_row): s = l / T_i, token = argmax of float(s + g) with g
+ * from noise stream 3 at position position[i] (argmax of s for a greedy
+ * row), probs = softmax(s) in double (one-hot for greedy).  T [R]: the rows'
+ * temperatures (finite and > 0); greedy, position: [R] or NULL (0).
+ * probs [R,V] double, rowstats [R,2] (M, S) and top2 [R,2] may be NULL.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_sample_temperature(const float* logits, const float* T,
+                              const uint8_t* greedy, const uint64_t* seed,
+                              const uint64_t* offset, const int32_t* position,
+                              int R, int V, int32_t* tokens, double* probs,
+                              double* rowstats, float* top2,
+                              double* probs_scratch) {
+  if (R <= 0 || V <= 0 || !logits || !T || !seed || !offset || !tokens ||
+      !probs_scratch)
+    return -1;
+  for (int i = 0; i < R; ++i) {
+    if (!(T[i] > 0.0f) || !isfinite(T[i])) return -1;
+    int pos = position ? position[i] : 0;
+    if (pos < 0 || pos > 0xffff) return -1;
+    double* q = probs ? probs + (size_t)i * V : probs_scratch;
+    int token;
+    double M, S;
+    float best, second;
+    oracle_sample_row(logits + (size_t)i * V, V, seed[i], offset[i], pos, 3,
+                      T[i], greedy ? greedy[i] != 0 : 0, q, &token, &M, &S,
+                      &best, &second);
+    tokens[i] = token;
+    if (rowstats) {
+      rowstats[2 * i] = M;
+      rowstats[2 * i + 1] = S;
+    }
+    if (top2) {
+      top2[2 * i] = best;
+      top2[2 * i + 1] = second;
     }
   }
   return 0;
