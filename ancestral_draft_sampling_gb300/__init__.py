@@ -16,7 +16,7 @@ from . import _lib
 from ._lib import BF16, F32, DsparkError  # noqa: F401
 
 __all__ = ["draft_block", "draft_block_per_request", "draft_block_noalloc",
-           "draft_block_profile",
+           "draft_block_profile", "sample_temperature",
            "draft_block_host", "HostWorkspace", "verify_standard", "verify_block",
            "noise_words", "workspace_bytes", "read_device_error",
            "DraftWorkspace", "DsparkError", "F32", "BF16", "version"]
@@ -294,6 +294,39 @@ def verify_block(draft_probs, target_probs, tokens, seed, offset, *,
     Returns (accepted_len, emitted)."""
     return _verify("dspark_verify_block", draft_probs, target_probs, tokens,
                    seed, offset, accepted_len, emitted_token, stream)
+
+
+def sample_temperature(logits, seed, offset, *, T: float = 1.0,
+                       temperature=None, greedy=None, position=None,
+                       tokens=None, probs=None, with_probs: bool = True,
+                       workspace=None, stream=None):
+    """Temperature-only sampling of target rows: logits [R, V] float32 on
+    the device, seed/offset [R] int64 (uint64 bit patterns), T (or
+    temperature [R] float32), greedy [R] uint8, position [R] int32.  Returns
+    (tokens [R], probs [R, V] or None).  See include/dspark.h."""
+    torch = _torch()
+    R, V = logits.shape
+    for t in (logits, seed, offset, temperature, greedy, position):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    dev = logits.device
+    if tokens is None:
+        tokens = torch.empty(R, dtype=torch.int32, device=dev)
+    if with_probs and probs is None:
+        probs = torch.empty((R, V), dtype=torch.float32, device=dev)
+    if not with_probs:
+        probs = None
+    nbytes = _lib.load().dspark_sample_workspace_bytes(R, V)
+    if nbytes == 0:
+        raise _lib.DsparkError("dspark_sample_workspace_bytes", 2)
+    if workspace is None or workspace.numel() < nbytes:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    st = _lib.load().dspark_sample_temperature(
+        _ptr(logits), _ptr(temperature), float(T), _ptr(greedy), _ptr(seed),
+        _ptr(offset), _ptr(position), R, V, _ptr(tokens), _ptr(probs),
+        _ptr(workspace), workspace.numel(), _stream(stream))
+    _lib.check("dspark_sample_temperature", st)
+    return tokens, probs
 
 
 def noise_words(seed: int, offset: int, k: int, stream_id: int, n: int,

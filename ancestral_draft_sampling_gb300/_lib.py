@@ -34,6 +34,8 @@ EXPORTED = (
     "dspark_draft_host_workspace_bytes",
     "dspark_draft_block_host",
     "dspark_verify_standard",
+    "dspark_sample_workspace_bytes",
+    "dspark_sample_temperature",
     "dspark_verify_block",
     "dspark_noise_words",
     "dspark_read_device_error",
@@ -92,6 +94,11 @@ def load() -> ctypes.CDLL:
             P, I, P, P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, I, P,
             ctypes.c_size_t, P]
         lib.dspark_draft_block_per_request.restype = I
+        lib.dspark_sample_workspace_bytes.argtypes = [I, I]
+        lib.dspark_sample_workspace_bytes.restype = ctypes.c_size_t
+        lib.dspark_sample_temperature.argtypes = [
+            P, P, ctypes.c_float, P, P, P, P, I, I, P, P, P, ctypes.c_size_t, P]
+        lib.dspark_sample_temperature.restype = I
         lib.dspark_noise_words.argtypes = [U64, U64, I, I, I, P, P, P]
         lib.dspark_noise_words.restype = I
         lib.dspark_read_device_error.argtypes = [P, P, P]

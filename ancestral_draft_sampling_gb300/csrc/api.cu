@@ -532,6 +532,61 @@ dspark_status dspark_verify_block(const float* draft_probs,
                      accepted_len, emitted_token, true, stream);
 }
 
+size_t dspark_sample_workspace_bytes(int R, int V) {
+  if (R < 1 || R > 65535 || V < 1 || V > DSPARK_MAX_V) return 0;
+  return workspace_layout(R, 1).total;
+}
+
+dspark_status dspark_sample_temperature(
+    const float* logits, const float* temperature, float T,
+    const uint8_t* greedy, const uint64_t* seed, const uint64_t* offset,
+    const int32_t* position, int R, int V, int32_t* tokens, float* probs,
+    void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (R <= 0 || V <= 0 || !logits || !seed || !offset || !tokens)
+    return DSPARK_ERR_INVALID_ARG;
+  if (!temperature && (!(T > 0.0f) || !std::isfinite(T)))
+    return DSPARK_ERR_INVALID_ARG;
+  const void* ptrs16[] = {logits, seed, offset, tokens, probs, workspace};
+  for (const void* p : ptrs16)
+    if (p && !aligned16(p)) return DSPARK_ERR_INVALID_ARG;
+  const void* ptrs4[] = {temperature, position};
+  for (const void* p : ptrs4)
+    if (p && (reinterpret_cast<uintptr_t>(p) & 3u) != 0)
+      return DSPARK_ERR_INVALID_ARG;
+  if (R > 65535 || V > DSPARK_MAX_V) return DSPARK_ERR_UNSUPPORTED;
+  const WorkspaceLayout L = workspace_layout(R, 1);
+  if (!workspace || workspace_bytes < L.total ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+    return DSPARK_ERR_WORKSPACE;
+  // rows as requests of a one-position block: the pick and the proposal
+  // writer of the draft block finish the rows
+  DraftArgs a{};
+  a.logits = const_cast<float*>(logits);
+  a.probs = probs;
+  a.tokens = tokens;
+  a.seed = seed;
+  a.offset = offset;
+  a.greedy = greedy;
+  a.T = temperature ? 1.0f : T;
+  a.temperature = temperature;
+  a.B = R;
+  a.K = 1;
+  a.V = V;
+  a.r = 16;
+  char* ws = static_cast<char*>(workspace);
+  a.stats = reinterpret_cast<ChunkStat*>(ws + L.stats);
+  a.rowstats = reinterpret_cast<float*>(ws + L.rowstats);
+  a.hints = reinterpret_cast<unsigned long long*>(ws + L.hints);
+  a.control = reinterpret_cast<int*>(ws + L.control);
+  const int sms = sm_count();
+  const int n_chunks = sample_chunks(R, V, sms);
+  dspark_status st = from_cuda(launch_sample_stats(a, position, n_chunks, stream));
+  if (st != DSPARK_OK) return st;
+  st = from_cuda(launch_pick(a, 0, n_chunks, 0, false, false, stream));
+  if (st != DSPARK_OK || !probs) return st;
+  return from_cuda(launch_proposals(a, 0, 1, stream));
+}
+
 dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,
                                  int stream_id, int n, uint32_t* out,
                                  float* gumbel, cudaStream_t stream) {

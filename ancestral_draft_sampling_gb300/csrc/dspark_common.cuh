@@ -23,6 +23,7 @@ constexpr int kNoIndex = 0x7fffffff;   // "no non-NaN candidate yet"
 constexpr int kNoiseDraft = 0;         // counter stream ids
 constexpr int kNoiseAccept = 1;
 constexpr int kNoiseResample = 2;
+constexpr int kNoiseTarget = 3;   // the temperature-only target sampler
 
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon et al., "Parallel random numbers: as easy as 1, 2,
@@ -222,6 +223,34 @@ __device__ __forceinline__ ChunkStat empty_stat() {
   return e;
 }
 
+// Folds four consecutive candidates v..v+3 into a lane's running statistic.
+__device__ __forceinline__ void fold4(ChunkStat& st, const float s[4],
+                                      const float score[4], int v, int V) {
+  float m4 = -INFINITY;
+  bool any_nan = false;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    if (v + e >= V) continue;
+    if (score[e] > st.best) {  // NaN and -inf never win
+      st.best = score[e];
+      st.idx = v + e;
+    }
+    m4 = fmaxf(m4, s[e]);
+    any_nan |= isnan(s[e]);
+  }
+  const float mn = fmaxf(st.m, m4);
+  if (mn == -INFINITY) {
+    if (any_nan) st.s = __int_as_float(0x7fc00000);
+  } else {
+    float acc = (st.m == mn) ? st.s : __fmul_rn(st.s, expf(st.m - mn));
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (v + e < V) acc = __fadd_rn(acc, expf(s[e] - mn));
+    st.s = acc;
+    st.m = mn;
+  }
+}
+
 // Float32 -> uint32 map that preserves order (for finite and infinite
 // values): flip every bit of negatives, set the sign bit of the others.
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
@@ -324,6 +353,7 @@ enum DeviceError : int {
   kDevErrTimeout = 2,   // a bounded wait inside a kernel ran out
   kDevErrBadTemperature = 3,  // a per-request temperature not finite and > 0
   kDevErrBadSlot = 4,   // a proposal slot outside [0, num_slots)
+  kDevErrBadPosition = 5,  // a sampler position outside [0, 65535] (0 used)
 };
 
 // ------------------------------------------------------- kernel launchers
@@ -387,6 +417,11 @@ cudaError_t launch_verify(const float* q, const float* p, const int32_t* tokens,
                           int K, int V, int32_t* accepted_len,
                           int32_t* emitted, int sms, bool block,
                           cudaStream_t stream);
+// Temperature-only sampler: chunk statistics of the rows of a.logits
+// (a.B rows, a.K == 1) into statistics buffer 0.
+int sample_chunks(int R, int V, int sm_count);
+cudaError_t launch_sample_stats(const DraftArgs& a, const int32_t* position,
+                                int n_chunks, cudaStream_t stream);
 cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
                                int stream_id, int n, uint32_t* out,
                                float* gumbel, cudaStream_t stream);

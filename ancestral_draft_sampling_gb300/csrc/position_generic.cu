@@ -88,34 +88,6 @@ __device__ __forceinline__ float scale(float l, float T) {
   return T == 1.0f ? l : __fdiv_rn(l, T);
 }
 
-// Folds four consecutive candidates v..v+3 into a lane's running statistic.
-__device__ __forceinline__ void fold4(ChunkStat& st, const float s[4],
-                                      const float score[4], int v, int V) {
-  float m4 = -INFINITY;
-  bool any_nan = false;
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    if (v + e >= V) continue;
-    if (score[e] > st.best) {  // NaN and -inf never win
-      st.best = score[e];
-      st.idx = v + e;
-    }
-    m4 = fmaxf(m4, s[e]);
-    any_nan |= isnan(s[e]);
-  }
-  const float mn = fmaxf(st.m, m4);
-  if (mn == -INFINITY) {
-    if (any_nan) st.s = __int_as_float(0x7fc00000);
-  } else {
-    float acc = (st.m == mn) ? st.s : __fmul_rn(st.s, expf(st.m - mn));
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (v + e < V) acc = __fadd_rn(acc, expf(s[e] - mn));
-    st.s = acc;
-    st.m = mn;
-  }
-}
-
 template <typename WT, typename BT, bool kVec>
 __global__ void __launch_bounds__(kThreads)
 position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {

@@ -408,7 +408,38 @@ def run_ours(args, rank, world):
     tl = torch.cat([logits, logits[:, -1:]], dim=1)
     tl = tl + torch.randn(tl.shape, device="cuda", generator=gen)
     target = torch.softmax(tl.nan_to_num(neginf=-1e30), dim=-1)
+    # temperature-only target sampling of the same B x (K+1) target rows
+    tl_rows = tl.reshape(B * (K + 1), V).contiguous()
     del tl
+    seed_rows = dev["seed"].repeat_interleave(K + 1)
+    off_rows = dev["offset"].repeat_interleave(K + 1)
+    pos_rows = torch.arange(K + 1, dtype=torch.int32, device="cuda").repeat(B)
+    smp_tok = torch.empty(B * (K + 1), dtype=torch.int32, device="cuda")
+    smp_probs = torch.empty_like(tl_rows)
+    smp_ws = torch.empty(pkg._lib.load().dspark_sample_workspace_bytes(B * (K + 1), V),
+                         dtype=torch.uint8, device="cuda")
+
+    def sample_call():
+        pkg.sample_temperature(tl_rows, seed_rows, off_rows, T=1.0,
+                               position=pos_rows, tokens=smp_tok,
+                               probs=smp_probs, workspace=smp_ws)
+
+    for _ in range(3):
+        sample_call()
+    torch.cuda.synchronize()
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    g0.record(cur)
+    for _ in range(10):
+        sample_call()
+    g1.record(cur)
+    torch.cuda.synchronize()
+    sampler = {"us_per_call": g0.elapsed_time(g1) / 10 * 1e3,
+               "rows": B * (K + 1), "V": V,
+               "bytes": 3 * B * (K + 1) * V * 4,
+               "note": "temperature-only sampling of the block's target rows "
+                       "(token and probabilities per row)"}
+    del tl_rows, smp_probs
     acc_len = torch.empty(B, dtype=torch.int32, device="cuda")
     emitted = torch.empty(B, dtype=torch.int32, device="cuda")
 
@@ -455,6 +486,7 @@ def run_ours(args, rank, world):
             "roofline": roofline,
             "clocks": clocks.summary(),
             "verify": verify,
+            "target_sampler": sampler,
             # kernels of one block (counted by the profile pass) x steps
             "gpu_launches": args.steps * sum(v[1] for v in prof.values()) // prof_reps,
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,

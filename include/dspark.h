@@ -316,6 +316,41 @@ DSPARK_API dspark_status dspark_verify_block(const float* draft_probs,
                                   cudaStream_t stream);
 
 /*
+ * dspark_sample_workspace_bytes -- device workspace of
+ * dspark_sample_temperature for R rows of V logits (0 if unsupported).
+ */
+DSPARK_API size_t dspark_sample_workspace_bytes(int R, int V);
+
+/*
+ * dspark_sample_temperature -- temperature-only sampling of target rows
+ * (PR #27, "1. Temperature-only sampling runs no filter": softmax and
+ * sampling, no top-k, top-p or min-p).
+ *
+ *   logits       [R,V] float32 device: one row per sample.
+ *   temperature  [R] float32 device (4-byte aligned) or NULL: per-row T (a
+ *                value that is not finite and positive counts as 1 and sets
+ *                the device error word to 3); NULL uses T (finite, > 0).
+ *   greedy       [R] uint8 or NULL: 1 = argmax of s, one-hot probabilities.
+ *   seed, offset [R] uint64: the row's noise key and counter words.
+ *   position     [R] int32 (4-byte aligned) or NULL (0): the counter's
+ *                position word, in [0, 65535] (outside: 0 is used and the
+ *                device error word is set to 5).
+ *   tokens       [R] int32 out; probs [R,V] float32 out, or NULL to skip.
+ *   workspace    dspark_sample_workspace_bytes(R, V) bytes, 256-byte aligned.
+ * Row i: s = l / T_i (float32 IEEE), token = argmax of s + g with g from
+ * noise stream 3 (word v & 3 of Philox4x32-10 block (v >> 2,
+ * position | 3 << 16, offset lo, offset hi) under key seed), the lowest
+ * index on ties, NaN never winning (a row where nothing wins gives token 0);
+ * probs = softmax(s).  R <= 65535.  Three launches on `stream`, graph
+ * capturable; results are reproducible call to call.
+ */
+DSPARK_API dspark_status dspark_sample_temperature(
+    const float* logits, const float* temperature, float T,
+    const uint8_t* greedy, const uint64_t* seed, const uint64_t* offset,
+    const int32_t* position, int R, int V, int32_t* tokens, float* probs,
+    void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * dspark_noise_words -- diagnostic: writes the n raw Philox words the
  * sampler uses for elements 0..n-1 of (seed, offset, position k, stream),
  * i.e. out[v] = word (v & 3) of Philox4x32-10(counter (v >> 2,
