@@ -181,3 +181,76 @@ def test_draft_block_host_rejects_bad_arguments(lib, over, want):
         a["K"], a["V"], a["r"], a["base_dev"], a["tokens"], a["logits"],
         a["probs"], a["ws"], a["ws_bytes"], a["stream"], a["copy_stream"])
     assert st == want
+
+
+def test_verify_block_rejects_bad_arguments(lib):
+    f = lib.dspark_verify_block
+    good = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 3, 100, FAKE, FAKE, None]
+    for i in [0, 1, 2, 3, 4, 8, 9]:
+        args = list(good)
+        args[i] = None
+        assert f(*args) == INVALID
+    for i, v in [(5, 0), (6, 0), (7, 0)]:
+        args = list(good)
+        args[i] = v
+        assert f(*args) == INVALID
+    args = list(good)
+    args[1] = FAKE + 8
+    assert f(*args) == INVALID
+    args = list(good)
+    args[6] = 65
+    assert f(*args) == UNSUPPORTED
+
+
+def _per_request_call(lib, a, temperature=FAKE, slot=None, num_slots=0):
+    return lib.dspark_draft_block_per_request(
+        a["base"], a["base_dtype"], a["U"], a["Wb"], a["w_dtype"], a["d0"],
+        a["seed"], a["offset"], temperature, a["greedy"], a["pad_row"], a["B"],
+        a["K"], a["V"], a["r"], a["tokens"], a["logits"], a["probs"], slot,
+        num_slots, a["workspace"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,over,want", [
+    (dict(temperature=None), {}, INVALID),          # the per-request values
+    (dict(temperature=FAKE + 2), {}, INVALID),      # 4-byte alignment
+    (dict(slot=FAKE, num_slots=0), {}, INVALID),    # slots need num_slots
+    (dict(slot=FAKE + 1, num_slots=8), {}, INVALID),
+    (dict(), dict(base=None), INVALID),             # the block's own checks
+    (dict(), dict(r=40), UNSUPPORTED),
+    (dict(), dict(ws_bytes=100), WORKSPACE),
+])
+def test_draft_block_per_request_rejects_bad_arguments(lib, kw, over, want):
+    assert _per_request_call(lib, _draft_args(lib, **over), **kw) == want
+
+
+def test_sample_workspace_bytes(lib):
+    f = lib.dspark_sample_workspace_bytes
+    assert f(704, 200064) > 0 and f(704, 200064) % 256 == 0
+    assert f(0, 100) == 0 and f(10, 0) == 0 and f(70000, 100) == 0
+
+
+def _sample_call(lib, **over):
+    R, V = 6, 1000
+    a = dict(logits=FAKE, temperature=None, T=1.0, greedy=None, seed=FAKE,
+             offset=FAKE, position=None, R=R, V=V, tokens=FAKE, probs=FAKE,
+             ws=FAKE, ws_bytes=lib.dspark_sample_workspace_bytes(R, V),
+             stream=None)
+    a.update(over)
+    return lib.dspark_sample_temperature(
+        a["logits"], a["temperature"], a["T"], a["greedy"], a["seed"],
+        a["offset"], a["position"], a["R"], a["V"], a["tokens"], a["probs"],
+        a["ws"], a["ws_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("over,want", [
+    (dict(logits=None), INVALID), (dict(seed=None), INVALID),
+    (dict(tokens=None), INVALID), (dict(R=0), INVALID), (dict(V=0), INVALID),
+    (dict(T=0.0), INVALID), (dict(T=float("nan")), INVALID),
+    (dict(logits=FAKE + 4), INVALID), (dict(position=FAKE + 2), INVALID),
+    (dict(temperature=FAKE + 1), INVALID),
+    (dict(R=70000), UNSUPPORTED),
+    (dict(ws=None), WORKSPACE), (dict(ws_bytes=64), WORKSPACE),
+    (dict(ws=FAKE + 16), WORKSPACE),
+])
+def test_sample_temperature_rejects_bad_arguments(lib, over, want):
+    assert _sample_call(lib, **over) == want
