@@ -13,13 +13,17 @@
 // pick kernel merges them into the token and the row's (M, S), and the
 // proposal writer writes softmax(s) (rows as requests, K = 1).
 //
-// Each thread keeps its best decision score ref (and index) and a sum
-// reference m (its largest s).  One exp2 per entry, f = exp(s - m), feeds the
-// sum and a conservative candidate test: an entry can beat ref only if its
-// Gumbel score does, i.e. only if w < exp(s - ref) = f exp(m - ref), which
-// the test (float)x < 2^32 (1 + 2^-11) f h, h = exp(m - ref), admits with
-// room for the rounding of both sides.  Only admitted entries get the exact
-// score s + g.
+// Each warp keeps one reference ref (the best decision score it has found,
+// and its index), the same in every lane; each thread keeps a sum reference
+// m (its largest s).  One exp2 per entry, f = exp(s - m), feeds the sum and a
+// conservative candidate test: an entry can beat ref only if its Gumbel
+// score does, i.e. only if w < exp(s - ref) = f exp(m - ref), which the test
+// (float)x < 2^32 (1 + 2^-11) f h, h = exp(m - ref), admits with room for the
+// rounding of both sides.  Only admitted entries get the exact score s + g,
+// and the warp then adopts the best of them.  With the reference shared by
+// the 32 lanes, a warp meets an admitted entry in a few of its steps only
+// (a reference per lane admitted one in most steps of some lane, and the
+// whole warp ran the exact path).
 #include "dspark_common.cuh"
 
 namespace dspark {
@@ -28,8 +32,13 @@ namespace {
 constexpr int kSampleThreads = 256;
 constexpr int kSampleWarps = kSampleThreads / 32;
 constexpr int kSampleBatch = 2;  // blocks a thread loads before using them
+constexpr int kSampleMinBlocks = 5;  // resident CTAs per SM (48 registers)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTestScale = 4297064448.0f;  // 2^32 (1 + 2^-11), exact in float32
+
+__device__ __forceinline__ float word_pick(const float (&a)[4], int e) {
+  return e == 0 ? a[0] : e == 1 ? a[1] : e == 2 ? a[2] : a[3];
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -37,10 +46,34 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// The best of the lanes' exact candidates (cb, ci) against the warp's
+// reference (ref, idx): the largest score by a max-reduction over
+// order-preserving bits, then the lowest index among the lanes that hold it.
+// A lane without a candidate offers key 0 (below every score).  Ties with
+// the reference keep the lower index.
+__device__ __forceinline__ bool warp_adopt(float& ref, int& idx, float cb,
+                                           int ci) {
+  const uint32_t key = ci == kNoIndex ? 0u : ordered_bits(cb);
+  const uint32_t kmax = __reduce_max_sync(0xffffffffu, key);
+  if (kmax == 0u) return false;
+  const uint32_t imin = __reduce_min_sync(
+      0xffffffffu, key == kmax ? (uint32_t)ci : 0xffffffffu);
+  const float wb = from_ordered_bits(kmax);
+  if (wb > ref || (wb == ref && (int)imin < idx)) {
+    ref = wb;
+    idx = (int)imin;
+    return true;
+  }
+  return false;
+}
+
 // grid (n_chunks, R): chunk c of row r covers the Philox blocks (4 entries
-// each) [c * chunk_blocks, (c + 1) * chunk_blocks).
-template <bool kVec>
-__global__ void __launch_bounds__(kSampleThreads)
+// each) [c * chunk_blocks, (c + 1) * chunk_blocks).  Thread t of the CTA
+// takes the blocks lo + t, lo + t + 256, ...; a warp's 32 lanes take 32
+// consecutive blocks at each step, and every warp runs the same number of
+// steps (lanes past the chunk's end see -inf entries).
+template <bool kVec, bool kUnitT>
+__global__ void __launch_bounds__(kSampleThreads, kSampleMinBlocks)
 sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
                     int chunk_blocks) {
   __shared__ uint4 s_pre, s_rk[4];
@@ -66,18 +99,19 @@ sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
   const int n_blk = (V + 3) / 4;
   const int lo = chunk * chunk_blocks;
   const int hi = min(lo + chunk_blocks, n_blk);
-  float ref = -INFINITY;  // best decision score of this thread
+  // sampled rows: the warp's reference; greedy rows: the lane's best
+  float ref = -INFINITY;
   int idx = kNoIndex;
   float m = -INFINITY;    // largest s of this thread: the sum's reference
   float sum = 0.0f;       // sum of exp(s - m)
   float h = INFINITY;     // exp(m - ref), used by the candidate test
   // kSampleBatch blocks per thread and step, every load issued first; the
   // blocks are then taken in the order j, j + threads, ... as one at a time
-  for (int j0 = lo + (int)threadIdx.x; j0 < hi; j0 += kSampleBatch * kSampleThreads) {
+  for (int base = lo; base < hi; base += kSampleBatch * kSampleThreads) {
     float lb[kSampleBatch][4];
 #pragma unroll
     for (int u = 0; u < kSampleBatch; ++u) {
-      const int j = j0 + u * kSampleThreads, v = 4 * j;
+      const int j = base + (int)threadIdx.x + u * kSampleThreads, v = 4 * j;
       if (j >= hi) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) lb[u][e] = -INFINITY;
@@ -95,12 +129,14 @@ sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
     }
 #pragma unroll
     for (int u = 0; u < kSampleBatch; ++u) {
-      const int j = j0 + u * kSampleThreads, v = 4 * j;
-      if (j >= hi) break;
+      const int j = base + (int)threadIdx.x + u * kSampleThreads, v = 4 * j;
+      // warp-uniform: the warp's first block is past the end
+      if (base + u * kSampleThreads + 32 * warp >= hi) break;
       const float* l = lb[u];
       float s[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[e] = T == 1.0f ? l[e] : __fdiv_rn(l[e], T);
+      for (int e = 0; e < 4; ++e)
+        s[e] = kUnitT || T == 1.0f ? l[e] : __fdiv_rn(l[e], T);
       // the sum's reference moves to a larger s (rare)
       float m4 = m;
 #pragma unroll
@@ -110,11 +146,12 @@ sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
         m = m4;
         h = ex2_approx((m - ref) * kLog2e);
       }
+      // exp(s - m); while m is -inf every s is -inf (term 0) or NaN (NaN),
+      // which the reference -FLT_MAX (the lowest finite float) gives as well
+      const float mr = fmaxf(m, -0x1.fffffep127f);
       float f[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e)  // -inf -> 0, NaN -> NaN
-        f[e] = m == -INFINITY ? (s[e] != s[e] ? s[e] : 0.0f)
-                              : ex2_approx((s[e] - m) * kLog2e);
+      for (int e = 0; e < 4; ++e) f[e] = ex2_approx((s[e] - mr) * kLog2e);
       sum = __fadd_rn(sum, __fadd_rn(__fadd_rn(f[0], f[1]), __fadd_rn(f[2], f[3])));
       if (greedy) {
 #pragma unroll
@@ -126,17 +163,23 @@ sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
       } else {
         const uint4 w = philox_folded(s_pre, s_rk, (uint32_t)j);
         const float c = kTestScale * h;
+        uint32_t cand = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t x = word_of(w, e);
-          if (__uint2float_rz(x) < __fmul_ru(f[e], c)) {  // a possible winner
-            const float sc = __fadd_rn(s[e], gumbel_from_word(x));
-            if (sc > ref) {
-              ref = sc;
-              idx = v + e;
-              h = ex2_approx((m - ref) * kLog2e);
+        for (int e = 0; e < 4; ++e)
+          cand |= (__uint2float_rz(word_of(w, e)) < __fmul_ru(f[e], c) ? 1u : 0u) << e;
+        if (__any_sync(0xffffffffu, cand != 0u)) {  // a possible winner
+          float cb = -INFINITY;
+          int ci = kNoIndex;
+          while (cand) {
+            const int e = __ffs(cand) - 1;
+            cand &= cand - 1u;
+            const float sc = __fadd_rn(word_pick(s, e), gumbel_from_word(word_of(w, e)));
+            if (sc > cb) {  // e ascending: strict keeps the lower index
+              cb = sc;
+              ci = v + e;
             }
           }
+          if (warp_adopt(ref, idx, cb, ci)) h = ex2_approx((m - ref) * kLog2e);
         }
       }
     }
@@ -173,12 +216,12 @@ cudaError_t launch_sample_stats(const DraftArgs& a, const int32_t* position,
   const int n_blk = (a.V + 3) / 4;
   const int chunk_blocks = (n_blk + n_chunks - 1) / n_chunks;
   const dim3 grid((unsigned)n_chunks, (unsigned)a.B, 1);
-  if (a.V % 4 == 0)
-    sample_stats_kernel<true><<<grid, kSampleThreads, 0, stream>>>(a, position,
-                                                                  chunk_blocks);
-  else
-    sample_stats_kernel<false><<<grid, kSampleThreads, 0, stream>>>(a, position,
-                                                                   chunk_blocks);
+  const bool unit = a.temperature == nullptr && a.T == 1.0f;
+  auto k = a.V % 4 == 0 ? (unit ? sample_stats_kernel<true, true>
+                                : sample_stats_kernel<true, false>)
+                        : (unit ? sample_stats_kernel<false, true>
+                                : sample_stats_kernel<false, false>);
+  k<<<grid, kSampleThreads, 0, stream>>>(a, position, chunk_blocks);
   return cudaGetLastError();
 }
 
