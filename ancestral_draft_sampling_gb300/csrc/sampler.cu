@@ -138,9 +138,7 @@ sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
       for (int e = 0; e < 4; ++e)
         s[e] = kUnitT || T == 1.0f ? l[e] : __fdiv_rn(l[e], T);
       // the sum's reference moves to a larger s (rare)
-      float m4 = m;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) m4 = s[e] > m4 ? s[e] : m4;  // NaN ignored
+      const float m4 = fmaxf(fmaxf(m, s[0]), fmaxf(fmaxf(s[1], s[2]), s[3]));  // NaN ignored
       if (m4 > m) {
         sum = __fmul_rn(sum, ex2_approx((m - m4) * kLog2e));  // 0 from -inf
         m = m4;
@@ -163,11 +161,17 @@ sample_stats_kernel(DraftArgs a, const int32_t* __restrict__ position,
       } else {
         const uint4 w = philox_folded(s_pre, s_rk, (uint32_t)j);
         const float c = kTestScale * h;
-        uint32_t cand = 0;
+        // the warp-wide vote needs only whether some entry passes; which
+        // ones pass is worked out on the rare path
+        const bool any = (__uint2float_rz(w.x) < __fmul_ru(f[0], c)) |
+                         (__uint2float_rz(w.y) < __fmul_ru(f[1], c)) |
+                         (__uint2float_rz(w.z) < __fmul_ru(f[2], c)) |
+                         (__uint2float_rz(w.w) < __fmul_ru(f[3], c));
+        if (__any_sync(0xffffffffu, any)) {  // a possible winner
+          uint32_t cand = 0;
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          cand |= (__uint2float_rz(word_of(w, e)) < __fmul_ru(f[e], c) ? 1u : 0u) << e;
-        if (__any_sync(0xffffffffu, cand != 0u)) {  // a possible winner
+          for (int e = 0; e < 4; ++e)
+            cand |= (__uint2float_rz(word_of(w, e)) < __fmul_ru(f[e], c) ? 1u : 0u) << e;
           float cb = -INFINITY;
           int ci = kNoIndex;
           while (cand) {
