@@ -97,9 +97,19 @@ __device__ __forceinline__ void load_block(const float* __restrict__ p,
   }
 }
 
+// The candidate test's scale for the warp's best: 2^32 (1 + slack)
+// e^-best; +inf (everything is a candidate) while nothing has won or e^-best
+// is out of float32's normal range.  It changes only when the best does.
+__device__ __forceinline__ float test_scale(const Best& st) {
+  return (st.idx == kNoIndex || st.score > kMaxTestScore)
+             ? INFINITY
+             : 0x1p32f * kSlack * expf(-st.score);
+}
+
 // One Philox block of the sweep: weights, candidate test, exact scores of
-// the candidates, warp merge.  Warp-uniform control flow.
-__device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
+// the candidates, warp merge.  Warp-uniform control flow.  c is
+// test_scale(st), kept up to date here.
+__device__ __forceinline__ void sweep_block(Best& st, float& c, bool& any, int j,
                                             float4 pv, float4 qv, bool resid,
                                             float wscale, const uint4& pre,
                                             const uint4 (&rk)[4]) {
@@ -112,18 +122,18 @@ __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
     any |= wt[e] > 0.0f;
   }
   const uint4 w = philox_folded(pre, rk, (uint32_t)j);
-  // 2^32 (1 + slack) e^-best; +inf (everything is a candidate) while nothing
-  // has won or e^-best is out of float32's normal range
-  const float c = (st.idx == kNoIndex || st.score > kMaxTestScore)
-                      ? INFINITY
-                      : 0x1p32f * kSlack * expf(-st.score);
-  uint32_t cand = 0;
+  float thr[4];
 #pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float thr = wt[e] > 0.0f ? __fmul_ru(wt[e], c) : 0.0f;
-    cand |= (__uint2float_rz(word_of(w, e)) < thr ? 1u : 0u) << e;
-  }
-  if (__any_sync(0xffffffffu, cand != 0u)) {
+  for (int e = 0; e < 4; ++e) thr[e] = wt[e] > 0.0f ? __fmul_ru(wt[e], c) : 0.0f;
+  // the vote needs only whether some entry passes; the rare path works out
+  // which ones do
+  const bool pass = (__uint2float_rz(w.x) < thr[0]) | (__uint2float_rz(w.y) < thr[1]) |
+                    (__uint2float_rz(w.z) < thr[2]) | (__uint2float_rz(w.w) < thr[3]);
+  if (__any_sync(0xffffffffu, pass)) {
+    uint32_t cand = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      cand |= (__uint2float_rz(word_of(w, e)) < thr[e] ? 1u : 0u) << e;
     float cb = -INFINITY;
     int ci = kNoIndex;
 #pragma unroll
@@ -136,6 +146,7 @@ __device__ __forceinline__ void sweep_block(Best& st, bool& any, int j,
       }
     }
     warp_take(st, cb, ci);
+    c = test_scale(st);
   }
 }
 
@@ -153,6 +164,7 @@ __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const bool resid = q != nullptr;
   Best st = {-INFINITY, kNoIndex};
+  float c = test_scale(st);
   bool any = false;
   constexpr int kStride = kVerifyWarps * 32;
   // two blocks per lane in flight: j and j + kStride
@@ -161,9 +173,9 @@ __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p
     float4 p0, q0, p1, q1;
     load_block<kVec>(p, q, V, j0, hi, p0, q0);
     load_block<kVec>(p, q, V, j1, hi, p1, q1);
-    sweep_block(st, any, j0, p0, q0, resid, wscale, pre, rk);
+    sweep_block(st, c, any, j0, p0, q0, resid, wscale, pre, rk);
     if (base + kStride < hi)
-      sweep_block(st, any, j1, p1, q1, resid, wscale, pre, rk);
+      sweep_block(st, c, any, j1, p1, q1, resid, wscale, pre, rk);
   }
   any = __any_sync(0xffffffffu, any);
   if (lane == 0) {
