@@ -26,7 +26,7 @@
  *     verification rule is standard token-level rejection sampling; the
  *     block rule is the block verification of Sun et al. (2024).
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - Philox variant: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel
  *     random numbers: as easy as 1, 2, 3", SC'11).
  *   - Counter layout: key = (seed lo, seed hi); counter =
