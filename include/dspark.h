@@ -341,8 +341,8 @@ DSPARK_API size_t dspark_sample_workspace_bytes(int R, int V);
  * noise stream 3 (word v & 3 of Philox4x32-10 block (v >> 2,
  * position | 3 << 16, offset lo, offset hi) under key seed), the lowest
  * index on ties, NaN never winning (a row where nothing wins gives token 0);
- * probs = softmax(s).  R <= 65535.  Three launches on `stream`, graph
- * capturable; results are reproducible call to call.
+ * probs = softmax(s).  R <= 65535.  Three launches on `stream` (two when
+ * probs is NULL), graph capturable; results are reproducible call to call.
  */
 DSPARK_API dspark_status dspark_sample_temperature(
     const float* logits, const float* temperature, float T,
