@@ -85,26 +85,45 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, period_ms: int = 20):
         self.gpu = gpu_index
+        self.period_ms = period_ms
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host monotonic arrival time, csv line)
+        self.t_start = None
+        self.t_stop = None
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.period_ms)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self._t = threading.Thread(target=self._read, daemon=True)
             self._t.start()
         except OSError:
             self.proc = None
+            return self
+        # nvidia-smi takes a moment to start: wait (bounded) for its first
+        # line so that sampling is live before the timed region opens
+        deadline = time.monotonic() + 5.0
+        while not self.lines and time.monotonic() < deadline and self.proc.poll() is None:
+            time.sleep(0.005)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
+
+    def start(self):
+        """Marks the opening of the timed region (host clock)."""
+        self.t_start = time.monotonic()
+
+    def stop(self):
+        """Marks the close of the timed region, after its synchronize."""
+        self.t_stop = time.monotonic()
+        # one more period so the sample taken at the close is read
+        time.sleep(2 * self.period_ms / 1000.0)
 
     def __exit__(self, *exc):
         if self.proc:
@@ -116,8 +135,23 @@ class ClockSampler:
             self._t.join(timeout=2)
 
     def summary(self):
+        lines = self.lines
+        window = "whole sampler lifetime"
+        if self.t_start is not None and self.t_stop is not None:
+            # keep only the samples read while the timed region ran; a line
+            # is read shortly after its query, hence the one-period slack
+            slack = self.period_ms / 1000.0
+            inside = [(t, ln) for t, ln in lines
+                      if self.t_start <= t <= self.t_stop + slack]
+            window = "timed region"
+            if not inside:
+                # region shorter than the sampling period: the first sample
+                # read after it opened
+                inside = [(t, ln) for t, ln in lines if t >= self.t_start][:1]
+                window = "first sample after the timed region opened"
+            lines = inside
         rows = []
-        for ln in self.lines:
+        for _, ln in lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 9:
                 continue
@@ -127,14 +161,15 @@ class ClockSampler:
                 continue
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
-                    "samples": 0}
+                    "samples": 0, "window": window}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                  "sw_power_cap"]
         reasons = sorted({names[i] for _, _, flags in rows
                           for i, f in enumerate(flags) if f.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows),
                 "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
-                "samples": len(rows)}
+                "samples": len(rows), "period_ms": self.period_ms,
+                "window": window}
 
 
 def source_hash(names):
@@ -316,11 +351,13 @@ def run_ours(args, rank, world):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         torch.cuda.synchronize()
+        clocks.start()
         ev0.record(cur)
         for _ in range(args.steps):
             graph.replay()
         ev1.record(cur)
         torch.cuda.synchronize()
+        clocks.stop()
     ms_step, us_per_block = job_timing(ev0.elapsed_time(ev1), args.steps,
                                        world, dist, "cuda")
 
