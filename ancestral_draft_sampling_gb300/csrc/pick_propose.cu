@@ -55,14 +55,21 @@ __device__ __forceinline__ float scale(float l, float T) {
   return T == 1.0f ? l : __fdiv_rn(l, T);
 }
 
-// grid = (B * k_count rows, segments of a row) for positions k_first ..
-// k_first + k_count - 1.  q = exp(s - M) * (1 / S).  Every load of a thread
-// is issued before its first store.
+// One CTA per (row, segment of a row) for positions k_first .. k_first +
+// k_count - 1, in a 1-D grid of B * k_count * n_seg CTAs.  The CTAs visit the
+// rows of the last position first and, within a row, the highest segment
+// first: the position kernel writes its vocab tiles in ascending order, so
+// the logits it wrote last are re-read first, while they are still in L2.
+// q = exp(s - M) * (1 / S).  Every load of a thread is issued before its
+// first store.
 template <bool kVec>
 __global__ void __launch_bounds__(kPropThreads)
-proposals_kernel(DraftArgs a, int k_first, int k_count) {
-  const int b = blockIdx.x / k_count;
-  const int row = b * a.K + k_first + (int)(blockIdx.x - b * k_count);
+proposals_kernel(DraftArgs a, int k_first, int k_count, int n_seg) {
+  const int visit = (int)blockIdx.x / n_seg;        // row in visiting order
+  const int seg_idx = n_seg - 1 - ((int)blockIdx.x - visit * n_seg);
+  const int kk = k_count - 1 - visit / a.B;          // last position first
+  const int b = visit - (visit / a.B) * a.B;
+  const int row = b * a.K + k_first + kk;
   const int V = a.V;
   const float M = a.rowstats[2 * (size_t)row];
   const float invS = __frcp_rn(a.rowstats[2 * (size_t)row + 1]);
@@ -75,18 +82,18 @@ proposals_kernel(DraftArgs a, int k_first, int k_count) {
   if (a.slot != nullptr) {
     dst = a.slot[b];
     if (dst < 0 || dst >= a.num_slots) {  // nothing is written for it
-      if (k == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+      if (k == 0 && seg_idx == 0 && threadIdx.x == 0)
         a.control[0] = kDevErrBadSlot;
       return;
     }
   }
   float* __restrict__ qrow = a.probs + ((size_t)dst * a.K + k) * V;
   const float T = request_temperature(a, b);
-  if (a.temperature != nullptr && k == 0 && blockIdx.y == 0 && threadIdx.x == 0 &&
+  if (a.temperature != nullptr && k == 0 && seg_idx == 0 && threadIdx.x == 0 &&
       T == 1.0f && a.temperature[b] != 1.0f)  // not finite and positive
     a.control[0] = kDevErrBadTemperature;
   const int seg = kPropThreads * kPropPerThread;
-  const int v_begin = blockIdx.y * seg;
+  const int v_begin = seg_idx * seg;
   if (kVec) {
     float4 l[kPropN4];
 #pragma unroll
@@ -154,11 +161,14 @@ cudaError_t launch_pick(const DraftArgs& a, int k, int n_chunks, int buf,
 cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,
                              cudaStream_t stream) {
   const int seg = kPropThreads * kPropPerThread;
-  const dim3 grid(a.B * k_count, (a.V + seg - 1) / seg);
+  const int n_seg = (a.V + seg - 1) / seg;
+  const long long ctas = (long long)a.B * k_count * n_seg;
+  if (ctas > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  const dim3 grid((unsigned)ctas);
   if (a.V % 4 == 0)
-    proposals_kernel<true><<<grid, kPropThreads, 0, stream>>>(a, k_first, k_count);
+    proposals_kernel<true><<<grid, kPropThreads, 0, stream>>>(a, k_first, k_count, n_seg);
   else
-    proposals_kernel<false><<<grid, kPropThreads, 0, stream>>>(a, k_first, k_count);
+    proposals_kernel<false><<<grid, kPropThreads, 0, stream>>>(a, k_first, k_count, n_seg);
   return cudaGetLastError();
 }
 
