@@ -16,7 +16,7 @@ from . import _lib
 from ._lib import BF16, F32, DsparkError  # noqa: F401
 
 __all__ = ["draft_block", "draft_block_per_request", "draft_block_noalloc",
-           "draft_block_profile", "sample_temperature",
+           "draft_block_profile", "draft_block_timeline", "sample_temperature",
            "draft_block_host", "HostWorkspace", "verify_standard", "verify_block",
            "noise_words", "workspace_bytes", "read_device_error",
            "DraftWorkspace", "DsparkError", "F32", "BF16", "version"]
@@ -69,6 +69,45 @@ class DraftWorkspace:
                                   device=device or "cuda")
 
 
+def _check_draft_inputs(base_logits, U, Wb, d0, seed, offset, greedy,
+                        pad_row, tokens=None, logits=None, draft_probs=None):
+    """Shapes, dtypes and contiguity of draft_block's tensors; returns
+    (B, K, V, r)."""
+    torch = _torch()
+    if base_logits.dim() != 3:
+        raise ValueError("base_logits must be [B, K, V]")
+    B, K, V = base_logits.shape
+    if U.dim() != 2:
+        raise ValueError("U must be [V, r]")
+    r = U.shape[1]
+    if tuple(U.shape) != (V, r) or tuple(Wb.shape) != (r, V):
+        raise ValueError("U must be [V, r] and Wb [r, V]")
+    if U.dtype != Wb.dtype:
+        raise TypeError("U and Wb must share a dtype")
+    _dtype_code(base_logits)
+    _dtype_code(U)
+    if d0.dtype != torch.int32 or tuple(d0.shape) != (B,):
+        raise TypeError("d0 must be int32 [B]")
+    for name, t in (("seed", seed), ("offset", offset)):
+        if t.dtype != torch.int64 or tuple(t.shape) != (B,):
+            raise TypeError(f"{name} must be int64 [B] (uint64 bit patterns)")
+    for name, t in (("greedy", greedy), ("pad_row", pad_row)):
+        if t is not None and (t.dtype != torch.uint8 or tuple(t.shape) != (B,)):
+            raise TypeError(f"{name} must be uint8 [B] or None")
+    if tokens is not None and (tokens.dtype != torch.int32 or
+                               tuple(tokens.shape) != (B, K)):
+        raise TypeError("tokens must be int32 [B, K]")
+    for name, t in (("logits", logits), ("draft_probs", draft_probs)):
+        if t is not None and (t.dtype != torch.float32 or
+                              tuple(t.shape) != (B, K, V)):
+            raise TypeError(f"{name} must be float32 [B, K, V]")
+    for t in (base_logits, U, Wb, d0, seed, offset, greedy, pad_row, tokens,
+              logits, draft_probs):
+        if t is not None and not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    return B, K, V, r
+
+
 def draft_block(base_logits, U, Wb, d0, seed, offset, T: float, *,
                 greedy=None, pad_row=None, tokens=None, logits=None,
                 draft_probs=None, workspace: Optional[DraftWorkspace] = None,
@@ -80,15 +119,9 @@ def draft_block(base_logits, U, Wb, d0, seed, offset, T: float, *,
     greedy/pad_row [B] uint8 or None.  Returns (tokens, logits, draft_probs).
     """
     torch = _torch()
-    B, K, V = base_logits.shape
-    r = U.shape[1]
-    if tuple(U.shape) != (V, r) or tuple(Wb.shape) != (r, V):
-        raise ValueError("U must be [V, r] and Wb [r, V]")
-    if U.dtype != Wb.dtype:
-        raise TypeError("U and Wb must share a dtype")
-    for t in (base_logits, U, Wb, d0, seed, offset, greedy, pad_row):
-        if t is not None and not t.is_contiguous():
-            raise ValueError("all tensors must be contiguous")
+    B, K, V, r = _check_draft_inputs(base_logits, U, Wb, d0, seed, offset,
+                                     greedy, pad_row, tokens, logits,
+                                     draft_probs)
     dev = base_logits.device
     if tokens is None:
         tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
@@ -208,12 +241,15 @@ def draft_block_noalloc(base_logits, U, Wb, d0, seed, offset, T: float, *,
                         greedy=None, pad_row=None, tokens=None, logits=None,
                         draft_probs=None, stream=None):
     """dspark_draft_block_noalloc: the draft block with library-owned scratch
-    instead of a caller-provided workspace (for callers that cannot allocate
-    device memory).  Outputs must be passed in; nothing is allocated here
-    either when they are."""
+    instead of a caller-provided workspace, for callers that cannot allocate
+    device memory.  The library call itself allocates nothing.  Outputs that
+    are not passed in are allocated here by torch, for convenience; a caller
+    that must not allocate passes tokens, logits and draft_probs.  Returns
+    (tokens, logits, draft_probs)."""
     torch = _torch()
-    B, K, V = base_logits.shape
-    r = U.shape[1]
+    B, K, V, r = _check_draft_inputs(base_logits, U, Wb, d0, seed, offset,
+                                     greedy, pad_row, tokens, logits,
+                                     draft_probs)
     dev = base_logits.device
     if tokens is None:
         tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
@@ -237,8 +273,9 @@ def draft_block_profile(base_logits, U, Wb, d0, seed, offset, T: float, *,
     every launch and returns {class: (total_ms, launches)} for the classes
     "position", "pick" and "proposal" (synchronises; not capturable)."""
     torch = _torch()
-    B, K, V = base_logits.shape
-    r = U.shape[1]
+    B, K, V, r = _check_draft_inputs(base_logits, U, Wb, d0, seed, offset,
+                                     greedy, pad_row, tokens, logits,
+                                     draft_probs)
     dev = base_logits.device
     if tokens is None:
         tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
@@ -260,6 +297,40 @@ def draft_block_profile(base_logits, U, Wb, d0, seed, offset, T: float, *,
     _lib.check("dspark_draft_block_profile", st)
     names = ("position", "pick", "proposal")
     return {names[i]: (float(ms[i]), int(n[i])) for i in range(3)}
+
+
+def draft_block_timeline(base_logits, U, Wb, d0, seed, offset, T: float, *,
+                         replays: int, stream, greedy=None, pad_row=None,
+                         tokens=None, logits=None, draft_probs=None,
+                         workspace=None):
+    """dspark_draft_block_timeline: the block captured into a CUDA graph with
+    event nodes around the position chain and the proposal writer, replayed
+    ``replays`` times on ``stream`` (a created stream, not the default one).
+    Returns (chain_ms, proposal_ms), the mean per replay (synchronises)."""
+    torch = _torch()
+    B, K, V, r = _check_draft_inputs(base_logits, U, Wb, d0, seed, offset,
+                                     greedy, pad_row, tokens, logits,
+                                     draft_probs)
+    dev = base_logits.device
+    if tokens is None:
+        tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    if logits is None:
+        logits = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if draft_probs is None:
+        draft_probs = torch.empty((B, K, V), dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = DraftWorkspace(B, K, V, r, device=dev)
+    chain = ctypes.c_float(0.0)
+    prop = ctypes.c_float(0.0)
+    st = _lib.load().dspark_draft_block_timeline(
+        _ptr(base_logits), _dtype_code(base_logits), _ptr(U), _ptr(Wb),
+        _dtype_code(U), _ptr(d0), _ptr(seed), _ptr(offset), float(T),
+        _ptr(greedy), _ptr(pad_row), B, K, V, r, _ptr(tokens), _ptr(logits),
+        _ptr(draft_probs), _ptr(workspace.buffer), workspace.nbytes,
+        int(replays), ctypes.byref(chain), ctypes.byref(prop),
+        _stream(stream))
+    _lib.check("dspark_draft_block_timeline", st)
+    return float(chain.value), float(prop.value)
 
 
 def _verify(fn, draft_probs, target_probs, tokens, seed, offset,
@@ -330,16 +401,20 @@ def sample_temperature(logits, seed, offset, *, T: float = 1.0,
 
 
 def noise_words(seed: int, offset: int, k: int, stream_id: int, n: int,
-                device=None, with_gumbel: bool = True, stream=None):
+                device=None, with_gumbel: bool = True, stream=None,
+                folded: bool = False):
     """Diagnostic: the raw Philox words (and float32 Gumbel variates) the
-    kernels use for elements 0..n-1.  Returns (words int32-view, gumbel)."""
+    kernels use for elements 0..n-1.  folded=True computes them the way the
+    hot kernels do (dspark_noise_words_folded).  Returns (words int32-view,
+    gumbel)."""
     torch = _torch()
     dev = device or "cuda"
     out = torch.empty(n, dtype=torch.int32, device=dev)
     g = torch.empty(n, dtype=torch.float32, device=dev) if with_gumbel else None
-    st = _lib.load().dspark_noise_words(seed, offset, k, stream_id, n,
-                                        _ptr(out), _ptr(g), _stream(stream))
-    _lib.check("dspark_noise_words", st)
+    fn = "dspark_noise_words_folded" if folded else "dspark_noise_words"
+    st = getattr(_lib.load(), fn)(seed, offset, k, stream_id, n, _ptr(out),
+                                  _ptr(g), _stream(stream))
+    _lib.check(fn, st)
     return out, g
 
 

@@ -30,6 +30,7 @@ EXPORTED = (
     "dspark_draft_block_per_request",
     "dspark_draft_block",
     "dspark_draft_block_profile",
+    "dspark_draft_block_timeline",
     "dspark_draft_block_noalloc",
     "dspark_draft_host_workspace_bytes",
     "dspark_draft_block_host",
@@ -38,6 +39,7 @@ EXPORTED = (
     "dspark_sample_temperature",
     "dspark_verify_block",
     "dspark_noise_words",
+    "dspark_noise_words_folded",
     "dspark_read_device_error",
     "dspark_status_string",
     "dspark_version",
@@ -76,6 +78,10 @@ def load() -> ctypes.CDLL:
             P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
             P, ctypes.c_size_t, P, P, P]
         lib.dspark_draft_block_profile.restype = I
+        lib.dspark_draft_block_timeline.argtypes = [
+            P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
+            P, ctypes.c_size_t, I, P, P, P]
+        lib.dspark_draft_block_timeline.restype = I
         lib.dspark_draft_block_noalloc.argtypes = [
             P, I, P, P, I, P, P, P, ctypes.c_float, P, P, I, I, I, I, P, P, P,
             P]
@@ -101,6 +107,8 @@ def load() -> ctypes.CDLL:
         lib.dspark_sample_temperature.restype = I
         lib.dspark_noise_words.argtypes = [U64, U64, I, I, I, P, P, P]
         lib.dspark_noise_words.restype = I
+        lib.dspark_noise_words_folded.argtypes = [U64, U64, I, I, I, P, P, P]
+        lib.dspark_noise_words_folded.restype = I
         lib.dspark_read_device_error.argtypes = [P, P, P]
         lib.dspark_read_device_error.restype = I
         lib.dspark_status_string.argtypes = [I]

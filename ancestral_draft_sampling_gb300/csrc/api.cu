@@ -2,11 +2,12 @@
 // workspace layout and the launch sequence of one draft block.
 //
 // Launch sequence of dspark_draft_block (brb-nv/TensorRT-LLM PR #27,
-// "2. One fused kernel per draft position"): for k = 0..K-1, one position
-// kernel (bias, scaling, Gumbel-max, logits, chunk statistics) and one pick
-// kernel (token d_k, row max and sum-exp); then one proposal writer for all
-// positions.  2K+1 launches on the caller's stream, no host synchronisation,
-// so the whole call can be captured in a CUDA graph.
+// "2. One fused kernel per draft position"): one 2-D memset (the device
+// error word and the decision keys), then for k = 0..K-1 one position
+// kernel (bias, scaling, Gumbel-max, logits, chunk statistics), one pick
+// (token d_k, row max and sum-exp) after the last tensor-core position or
+// after every FFMA position, and one proposal writer for all positions.  No
+// host synchronisation, so the whole call can be captured in a CUDA graph.
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
@@ -172,9 +173,12 @@ struct HostFeed {
   cudaEvent_t* ready;     // K + 1 events
 };
 
-// The launch sequence of one draft block.
+// The launch sequence of one draft block.  chain_end (measurement only):
+// an event recorded as an external event node between the position chain
+// (the memset, the positions and their picks) and the proposal writer.
 dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
-                        StageTimer* t, const HostFeed* feed = nullptr) {
+                        StageTimer* t, const HostFeed* feed = nullptr,
+                        cudaEvent_t chain_end = nullptr) {
   const int sms = sm_count() < kMaxChunks ? sm_count() : kMaxChunks;
   const int choice = position_kernel_choice(a);
   if (choice < 0) return DSPARK_ERR_UNSUPPORTED;
@@ -183,10 +187,12 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   // merged in slot order
   const int want = tc ? position_tc_chunks(a.V, sms) : sms;
   const int n_chunks = tc ? want : generic_chunks_used(a.V, want);
-  // the decision keys of every position start at zero (no winner)
-  if (tc && cudaMemset2DAsync(a.hints, kHintRowKeys * sizeof(uint64_t), 0,
-                              (size_t)a.K * sizeof(uint64_t), a.B,
-                              stream) != cudaSuccess)
+  // One 2-D memset over the control row and the B key rows (one pitch):
+  // the device error word starts every block at 0, and the decision keys of
+  // every position at zero (no winner).
+  if (cudaMemset2DAsync(a.control, kHintRowBytes, 0,
+                        (size_t)a.K * sizeof(uint64_t), (size_t)a.B + 1,
+                        stream) != cudaSuccess)
     return DSPARK_ERR_CUDA;
   if (feed) {
     // position k's drafter logits: B rows of V values, K V apart
@@ -234,7 +240,63 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
     }
   }
   if (feed) return DSPARK_OK;
+  if (chain_end && cudaEventRecordWithFlags(chain_end, stream,
+                                            cudaEventRecordExternal) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   return timed_launch(t, 2, stream, proposals_adapter, a, 0, 0);
+}
+
+// dspark_draft_block_timeline: the block captured once into a CUDA graph
+// with event nodes at its start, between the position chain and the
+// proposal writer, and at its end; the graph is replayed and the two
+// segments timed per replay.
+dspark_status timeline(const DraftArgs& a, int replays, float* chain_ms,
+                       float* proposal_ms, cudaStream_t stream) {
+  cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  dspark_status st = DSPARK_OK;
+  for (int i = 0; i < 3 && st == DSPARK_OK; ++i)
+    if (cudaEventCreate(&ev[i]) != cudaSuccess) st = DSPARK_ERR_CUDA;
+  if (st == DSPARK_OK &&
+      cudaStreamBeginCapture(stream, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    st = DSPARK_ERR_CUDA;
+  if (st == DSPARK_OK) {
+    dspark_status cap = from_cuda(
+        cudaEventRecordWithFlags(ev[0], stream, cudaEventRecordExternal));
+    if (cap == DSPARK_OK) cap = run_block(a, stream, nullptr, nullptr, ev[1]);
+    if (cap == DSPARK_OK)
+      cap = from_cuda(
+          cudaEventRecordWithFlags(ev[2], stream, cudaEventRecordExternal));
+    // the capture is ended in every case, so the stream leaves capture mode
+    const cudaError_t end = cudaStreamEndCapture(stream, &graph);
+    st = cap != DSPARK_OK ? cap : from_cuda(end);
+  }
+  if (st == DSPARK_OK &&
+      cudaGraphInstantiate(&exec, graph, 0) != cudaSuccess)
+    st = DSPARK_ERR_CUDA;
+  double chain = 0.0, prop = 0.0;
+  for (int i = 0; i < replays && st == DSPARK_OK; ++i) {
+    float m0 = 0.0f, m1 = 0.0f;
+    if (cudaGraphLaunch(exec, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess ||
+        cudaEventElapsedTime(&m0, ev[0], ev[1]) != cudaSuccess ||
+        cudaEventElapsedTime(&m1, ev[1], ev[2]) != cudaSuccess) {
+      st = DSPARK_ERR_CUDA;
+      break;
+    }
+    chain += m0;
+    prop += m1;
+  }
+  if (st == DSPARK_OK) {
+    *chain_ms = (float)(chain / replays);
+    *proposal_ms = (float)(prop / replays);
+  }
+  if (exec) cudaGraphExecDestroy(exec);
+  if (graph) cudaGraphDestroy(graph);
+  for (int i = 0; i < 3; ++i)
+    if (ev[i]) cudaEventDestroy(ev[i]);
+  return st;
 }
 
 // Device workspace of dspark_draft_block_host: the draft workspace, then the
@@ -270,16 +332,23 @@ __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 // Device address of g_noalloc_scratch on the current device.  The symbol
 // name is a host-side stand-in, never a device address, so it is resolved
-// once per device (with that device current) and cached.
-cudaError_t noalloc_scratch(void** out) {
+// with the device current.  Outside stream capture it is looked up on every
+// call (cheap; a device reset or a new primary context moves it) and
+// cached per device; during a capture the cached address is used, so the
+// first call on a device must come before any capture.
+cudaError_t noalloc_scratch(cudaStream_t stream, void** out) {
   static std::mutex mu;
   static void* addr[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (cap == cudaStreamCaptureStatusNone || addr[dev] == nullptr) {
+    if (cap != cudaStreamCaptureStatusNone) return cudaErrorStreamCaptureUnsupported;
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
@@ -414,6 +483,25 @@ dspark_status dspark_draft_block_profile(
   return st;
 }
 
+dspark_status dspark_draft_block_timeline(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, int replays, float* chain_ms, float* proposal_ms,
+    cudaStream_t stream) {
+  if (!chain_ms || !proposal_ms || replays < 1 || stream == nullptr)
+    return DSPARK_ERR_INVALID_ARG;
+  DraftArgs a{};
+  dspark_status st = prepare_draft(
+      base_logits, base_dtype, U, Wb, w_dtype, d0, seed, offset, T, greedy,
+      pad_row, B, K, V, r, tokens, logits, draft_probs, workspace,
+      workspace_bytes, a);
+  if (st != DSPARK_OK) return st;
+  return timeline(a, replays, chain_ms, proposal_ms, stream);
+}
+
 dspark_status dspark_draft_block_noalloc(
     const void* base_logits, dspark_dtype base_dtype, const void* U,
     const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
@@ -429,15 +517,14 @@ dspark_status dspark_draft_block_noalloc(
       kNoallocScratchBytes, a);
   if (st != DSPARK_OK) return st;  // sizes past the scratch: WORKSPACE
   void* scratch = nullptr;
-  if (noalloc_scratch(&scratch) != cudaSuccess) return DSPARK_ERR_CUDA;
+  if (noalloc_scratch(stream, &scratch) != cudaSuccess) return DSPARK_ERR_CUDA;
   st = prepare_draft(base_logits, base_dtype, U, Wb, w_dtype, d0, seed,
                      offset, T, greedy, pad_row, B, K, V, r, tokens, logits,
                      draft_probs, scratch, kNoallocScratchBytes, a);
   if (st != DSPARK_OK) return st;
   // the scratch keeps the previous call's contents: only the device error
-  // word must start at zero (every other word is written before it is read)
-  if (cudaMemsetAsync(scratch, 0, sizeof(int), stream) != cudaSuccess)
-    return DSPARK_ERR_CUDA;
+  // word and the decision keys must start at zero, and the block's first
+  // launch clears them (every other word is written before it is read)
   return run_block(a, stream, nullptr);
 }
 
@@ -580,6 +667,9 @@ dspark_status dspark_sample_temperature(
   a.control = reinterpret_cast<int*>(ws + L.control);
   const int sms = sm_count();
   const int n_chunks = sample_chunks(R, V, sms);
+  // the device error word starts every call at 0
+  if (cudaMemsetAsync(a.control, 0, sizeof(int), stream) != cudaSuccess)
+    return DSPARK_ERR_CUDA;
   dspark_status st = from_cuda(launch_sample_stats(a, position, n_chunks, stream));
   if (st != DSPARK_OK) return st;
   st = from_cuda(launch_pick(a, 0, n_chunks, 0, false, false, stream));
@@ -587,16 +677,31 @@ dspark_status dspark_sample_temperature(
   return from_cuda(launch_proposals(a, 0, 1, stream));
 }
 
-dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,
-                                 int stream_id, int n, uint32_t* out,
-                                 float* gumbel, cudaStream_t stream) {
+namespace {
+dspark_status noise_words(uint64_t seed, uint64_t offset, int k, int stream_id,
+                          int n, uint32_t* out, float* gumbel, bool folded,
+                          cudaStream_t stream) {
   if (n <= 0 || !out || k < 0 || k > 0xffff || stream_id < 0 ||
       stream_id > 0xffff)
     return DSPARK_ERR_INVALID_ARG;
   if (!aligned16(out) || (gumbel && !aligned16(gumbel)))
     return DSPARK_ERR_INVALID_ARG;
-  return from_cuda(
-      launch_noise_words(seed, offset, k, stream_id, n, out, gumbel, stream));
+  return from_cuda(launch_noise_words(seed, offset, k, stream_id, n, out,
+                                      gumbel, folded, stream));
+}
+}  // namespace
+
+dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int k,
+                                 int stream_id, int n, uint32_t* out,
+                                 float* gumbel, cudaStream_t stream) {
+  return noise_words(seed, offset, k, stream_id, n, out, gumbel, false,
+                     stream);
+}
+
+dspark_status dspark_noise_words_folded(uint64_t seed, uint64_t offset, int k,
+                                        int stream_id, int n, uint32_t* out,
+                                        float* gumbel, cudaStream_t stream) {
+  return noise_words(seed, offset, k, stream_id, n, out, gumbel, true, stream);
 }
 
 dspark_status dspark_read_device_error(void* workspace, int* code,

@@ -316,14 +316,20 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 // at their L2 slices (4 KB apart measured 2 us faster per position than
 // 128 B apart).
 constexpr int kHintRowKeys = 512;
+constexpr size_t kHintRowBytes = kHintRowKeys * sizeof(uint64_t);
 
+// The control row (the device error word first) and the B key rows share
+// one pitch, so a single 2-D memset of width 8 K over B + 1 rows clears the
+// error word and the keys of every position at the start of a block.
 struct WorkspaceLayout {
-  size_t control;   // 256 B at offset 0: device error word and counters
+  size_t control;   // one key row at offset 0: int 0 is the device error
+                    // word (the rest of the row is unused)
+  size_t hints;     // [B] rows of kHintRowKeys uint64 right after it; key k
+                    // of row b is the best decision key posted for
+                    // (b, position k)
   size_t stats;     // [2, B, kMaxChunks] ChunkStat: two buffers, so that a
                     // position's statistics survive the next position
   size_t rowstats;  // [B, K, 2] float (M, S)
-  size_t hints;     // [B] rows of kHintRowKeys uint64; key k of row b is
-                    // the best decision key posted for (b, position k)
   size_t total;
 };
 
@@ -335,13 +341,13 @@ __host__ __device__ inline WorkspaceLayout workspace_layout(int B, int K) {
   WorkspaceLayout L;
   size_t off = 0;
   L.control = off;
-  off += 256;
+  off += kHintRowBytes;
+  L.hints = off;
+  off += (size_t)B * kHintRowBytes;
   L.stats = off;
   off = align_up(off + 2 * (size_t)B * kMaxChunks * sizeof(ChunkStat), 256);
   L.rowstats = off;
   off = align_up(off + (size_t)B * K * 2 * sizeof(float), 256);
-  L.hints = off;
-  off = align_up(off + (size_t)B * kHintRowKeys * sizeof(uint64_t), 256);
   L.total = off;
   return L;
 }
@@ -424,6 +430,7 @@ cudaError_t launch_sample_stats(const DraftArgs& a, const int32_t* position,
                                 int n_chunks, cudaStream_t stream);
 cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
                                int stream_id, int n, uint32_t* out,
-                               float* gumbel, cudaStream_t stream);
+                               float* gumbel, bool folded,
+                               cudaStream_t stream);
 
 }  // namespace dspark

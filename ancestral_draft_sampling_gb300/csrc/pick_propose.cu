@@ -129,12 +129,24 @@ proposals_kernel(DraftArgs a, int k_first, int k_count, int n_seg) {
 
 constexpr int kNoiseThreads = 256;
 
+// folded: the words come from philox_fold / philox_folded, the form the
+// position, verification and sampler kernels run (rounds 1-2 folded into
+// per-request constants); otherwise from the plain ten-round loop.
 __global__ void noise_words_kernel(uint64_t seed, uint64_t offset, int k,
                                    int stream_id, int n, uint32_t* out,
-                                   float* gumbel) {
+                                   float* gumbel, bool folded) {
   const int v = blockIdx.x * kNoiseThreads + threadIdx.x;
   if (v >= n) return;
-  const uint4 w = noise_block(seed, offset, k, stream_id, (uint32_t)v >> 2);
+  uint4 w;
+  if (folded) {
+    uint4 pre, rk[4];
+    philox_fold(pre, rk, (uint32_t)seed, (uint32_t)(seed >> 32),
+                (uint32_t)k | ((uint32_t)stream_id << 16), (uint32_t)offset,
+                (uint32_t)(offset >> 32));
+    w = philox_folded(pre, rk, (uint32_t)v >> 2);
+  } else {
+    w = noise_block(seed, offset, k, stream_id, (uint32_t)v >> 2);
+  }
   const uint32_t x = word_of(w, v & 3);
   out[v] = x;
   if (gumbel) gumbel[v] = gumbel_from_word(x);
@@ -174,9 +186,11 @@ cudaError_t launch_proposals(const DraftArgs& a, int k_first, int k_count,
 
 cudaError_t launch_noise_words(uint64_t seed, uint64_t offset, int k,
                                int stream_id, int n, uint32_t* out,
-                               float* gumbel, cudaStream_t stream) {
+                               float* gumbel, bool folded,
+                               cudaStream_t stream) {
   noise_words_kernel<<<(n + kNoiseThreads - 1) / kNoiseThreads, kNoiseThreads,
-                       0, stream>>>(seed, offset, k, stream_id, n, out, gumbel);
+                       0, stream>>>(seed, offset, k, stream_id, n, out, gumbel,
+                                    folded);
   return cudaGetLastError();
 }
 

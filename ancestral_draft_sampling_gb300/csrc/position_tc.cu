@@ -55,6 +55,7 @@
 // its in-flight copies and MMAs, frees its TMEM and returns.
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "dspark_common.cuh"
@@ -82,6 +83,7 @@ constexpr int kMaxRows = (kMaxBpad + kComputeWarps - 1) / kComputeWarps;  // req
 constexpr uint32_t kTmemCols = 256;                // two accumulators
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSpin = 1u << 22;
+constexpr uint32_t kStallPolls = 1u << 12;  // the stalled wait's poll limit
 constexpr int kMinStages = 3;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;              // 227 KB per CTA
@@ -112,6 +114,8 @@ struct TcParams {
   int bpad;
   int stages;
   int tiles_total;
+  int stall_first_wait;  // failure-path test: the MMA issuer's first wait is
+                         // on a phase nothing completes, with a short limit
   int n_chunks;
   uint32_t u_off, tile_off, stage_off, rows_off, rstate_off, bar_off;
 };
@@ -522,11 +526,14 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   // grid to finish before it reads the statistics
   if (threadIdx.x == 0) launch_dependents();
   const uint32_t tmem_base = *tmem_holder;
+  // loads issued by the two producers (warp 0, lanes 0 and 1): after an
+  // abort, the teardown waits for them to land before the CTA exits
+  int wb_issued = 0, base_issued = 0;
 
   if (warp == 0) {
     if (lane == 0) {
       // -------------------------------------------------- Wb producer
-      int g = 0;
+      int& g = wb_issued;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t) {
         const int v0 = (chunk + t * P.n_chunks) * kTileV;
         for (int kc = 0; kc < kchunks; ++kc, ++g) {
@@ -542,16 +549,10 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           tma_load_2d(dst + kBoxBytes, &wb_map, &full[s], v0 + 64, kc * kKChunk);
         }
       }
-      if (*abort_flag) {  // let every issued load land (bounded)
-        for (int s = 0; s < S && s < g; ++s) {
-          const int last = g - 1 - ((g - 1 - s) % S);
-          mbar_wait(&full[s], (uint32_t)(last / S) & 1u, kSpin >> 4);
-        }
-      }
     } else if (lane == 1) {
       // ----------------------------------------- drafter-logit producer
       const uint32_t bytes = (uint32_t)(tile_floats * (int)sizeof(BT));
-      int issued = 0;
+      int& issued = base_issued;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t, ++issued) {
         const int v0 = (chunk + t * P.n_chunks) * kTileV;
         if (kStaged) {
@@ -571,13 +572,6 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           tma_load_2d(tiles + (size_t)buf * tile_floats, &base_map, &base_full[buf], v0, 0);
         }
       }
-      if (*abort_flag) {  // let every issued load land (bounded)
-        for (int t = issued - 2 < 0 ? 0 : issued - 2; t < issued; ++t) {
-          const int buf = kStaged ? 0 : (t & 1);
-          const uint32_t ph = kStaged ? ((uint32_t)t & 1u) : ((uint32_t)(t >> 1) & 1u);
-          mbar_wait(&base_full[buf], ph, kSpin >> 4);
-        }
-      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -585,7 +579,9 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTileV, (uint32_t)P.bpad, 1u, 0u);
       const uint32_t u_base = smem_u32(u_s);
-      if (!mbar_wait(u_ready, 0u, kSpin)) fail(kDevErrTimeout);
+      if (!mbar_wait(u_ready, P.stall_first_wait ? 1u : 0u,
+                     P.stall_first_wait ? kStallPolls : kSpin))
+        fail(kDevErrTimeout);
       int g = 0;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t) {
         const int acc = t & 1;
@@ -956,9 +952,36 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
+  if (warp == 0 && *abort_flag) {
+    // after an abort, loads may have been issued that no consumer waited
+    // for: let each barrier's last issued load land (bounded) before the
+    // CTA's shared memory is released
+    if (lane == 0) {
+      for (int s = 0; s < S && s < wb_issued; ++s) {
+        const int last = wb_issued - 1 - ((wb_issued - 1 - s) % S);
+        mbar_wait(&full[s], (uint32_t)(last / S) & 1u, kSpin >> 4);
+      }
+    } else if (lane == 1 && base_issued > 0) {
+      if (kStaged) {  // one staging buffer: its last load is the latest phase
+        mbar_wait(&base_full[0], (uint32_t)(base_issued - 1) & 1u, kSpin >> 4);
+      } else {        // the last load of each of the two tile buffers
+        for (int t = base_issued - 2 < 0 ? 0 : base_issued - 2; t < base_issued; ++t)
+          mbar_wait(&base_full[t & 1], (uint32_t)(t >> 1) & 1u, kSpin >> 4);
+      }
+    }
+  }
 }
 
 // ------------------------------------------------------------ host side
+// DSPARK_TEST_STALL_WAIT=1 (tests of the failure path only): the MMA
+// issuer's first wait is made on a barrier phase that nothing completes,
+// with a short poll limit, so that it runs out, the kernel records
+// kDevErrTimeout and takes its abort path.  That wait guards no copy.
+bool stall_first_wait_requested() {
+  const char* env = std::getenv("DSPARK_TEST_STALL_WAIT");
+  return env != nullptr && env[0] == '1';
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1093,6 +1116,7 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
   P.k = k;
   P.bpad = L.bpad;
   P.stages = L.stages;
+  P.stall_first_wait = stall_first_wait_requested() ? 1 : 0;
   P.tiles_total = (a.V + kTileV - 1) / kTileV;
   P.n_chunks = n_chunks;
   P.u_off = L.u_off;

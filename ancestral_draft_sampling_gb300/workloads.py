@@ -191,6 +191,36 @@ def make_verify(B, K, V, *, seed=1, logit_std=3.0, target_noise=1.0,
                         offset=offs)
 
 
+def _tensor(a: np.ndarray, device):
+    """numpy -> torch on `device`: bf16 bit patterns (uint16) become
+    bfloat16 and uint64 becomes int64 with the same bits."""
+    import torch
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+    if a.dtype == np.uint64:
+        return torch.from_numpy(a.view(np.int64)).to(device)
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device)
+
+
+def to_device(w: Workload, device="cuda:0") -> dict:
+    """The workload's arrays as torch tensors on `device`, in the dtypes the
+    binding takes (base, U, Wb, d0 int32, seed/offset int64, greedy/pad_row
+    uint8 or None, and target when the workload has one)."""
+    d = {
+        "base": _tensor(w.base, device),
+        "U": _tensor(w.U, device),
+        "Wb": _tensor(w.Wb, device),
+        "d0": _tensor(w.d0.astype(np.int32), device),
+        "seed": _tensor(w.seed, device),
+        "offset": _tensor(w.offset, device),
+        "greedy": None if w.greedy is None else _tensor(w.greedy, device),
+        "pad_row": None if w.pad_row is None else _tensor(w.pad_row, device),
+    }
+    if w.target is not None:
+        d["target"] = _tensor(w.target, device)
+    return d
+
+
 CONFIG_NAMES = {1: "small", 2: "b8", 3: "b44", 4: "b88", 5: "b64v"}
 
 

@@ -1,16 +1,18 @@
 """Benchmark of the DSpark ancestral draft-block sampler on one GB300.
 
-One step = one whole K=7 draft block (every position kernel, pick and the
-proposal writer) over the B=88, V=200064, r=256 workload (float32 drafter
-logits, bfloat16 Markov head, T=1, requests 80..87 are CUDA-graph padding
-rows), replayed from a CUDA graph -- the configuration the throughput target
-is stated on.  Prints one JSON line.
+One step = one whole K=7 draft block (the memset of the error word and the
+decision keys, every position kernel, the pick and the proposal writer) over
+the B=88, V=200064, r=256 workload (float32 drafter logits, bfloat16 Markov
+head, T=1, requests 80..87 are CUDA-graph padding rows), replayed from a
+CUDA graph -- the configuration the throughput target is stated on.  Prints
+one JSON line.  The other full-size configurations (B = 8, 44, 64) are
+measured the same way under "per_config".
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle (test infrastructure) on the host cores
-on a bounded sample of the same workload.  Under torchrun (N > 1) every rank
-runs an independent replica (no collective on the path); rank 0 prints.
+on the whole block.  Under torchrun (N > 1) every rank runs an independent
+replica (no collective on the path); rank 0 prints.
 """
 from __future__ import annotations
 
@@ -85,8 +87,8 @@ class ClockSampler:
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, period_ms: int = 20):
-        self.gpu = gpu_index
+    def __init__(self, gpu_id: str, period_ms: int = 20):
+        self.gpu = gpu_id  # "GPU-<uuid>" (or an nvidia-smi index)
         self.period_ms = period_ms
         self.proc = None
         self.lines = []  # (host monotonic arrival time, csv line)
@@ -172,6 +174,20 @@ class ClockSampler:
                 "window": window}
 
 
+def nvsmi_gpu_id(local: int) -> str:
+    """The identity nvidia-smi knows this CUDA device by: "GPU-<uuid>" from
+    the device properties (CUDA_VISIBLE_DEVICES may renumber devices, so the
+    CUDA index is not nvidia-smi's index); the CUDA index as a fallback."""
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local).uuid)
+        if u and u != "None":
+            return u if u.startswith("GPU-") else "GPU-" + u
+    except (AttributeError, RuntimeError):
+        pass
+    return str(local)
+
+
 def source_hash(names):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ancestral_draft_sampling_gb300", "csrc")
@@ -213,10 +229,10 @@ def job_timing(ms_total_local, steps, world, dist=None, device="cpu"):
 
 
 # ------------------------------------------------------------ CPU oracle
-def oracle_block_seconds(w, n_requests: int, threads: int):
-    """Wall seconds for the oracle to draft `n_requests` requests (all K
-    positions each, in order) with `threads` host threads."""
-    import numpy as np
+def oracle_block_seconds(w, threads: int):
+    """Wall seconds for the oracle to draft the whole block (every request,
+    all K positions each, in order) with `threads` host threads, requests
+    dealt to the threads."""
     from concurrent.futures import ThreadPoolExecutor
 
     import oracle
@@ -232,10 +248,13 @@ def oracle_block_seconds(w, n_requests: int, threads: int):
             prev = res.token
         return prev
 
-    reqs = list(range(n_requests))
     t0 = time.perf_counter()
-    with ThreadPoolExecutor(max_workers=threads) as ex:
-        list(ex.map(one, reqs))
+    if threads == 1:
+        for b in range(w.B):
+            one(b)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(one, range(w.B)))
     return time.perf_counter() - t0
 
 
@@ -246,18 +265,19 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(w, budget_s: float = 20.0):
+def cpu_baseline(w):
+    """The oracle on the whole block: once with every host core (the
+    reported value) and once single-threaded."""
     threads = cpu_threads()
-    n = min(w.B, threads)
-    t = oracle_block_seconds(w, n, threads)
-    waves_full = -(-w.B // threads)
-    per_block_s = t * waves_full  # one wave of n <= threads requests took t
+    t_all = oracle_block_seconds(w, threads)
+    t_one = oracle_block_seconds(w, 1)
     return {
-        "value": per_block_s * 1e6, "unit": "us", "cores": threads,
+        "value": t_all * 1e6, "unit": "us", "cores": threads,
         "kind": "oracle",
-        "sample": (f"{n} of {w.B} requests x {w.K} positions in one parallel "
-                   f"wave ({t:.2f} s), scaled by {waves_full} waves to a full "
-                   f"block"),
+        "single_thread_us": t_one * 1e6,
+        "sample": (f"the whole block ({w.B} requests x {w.K} positions) "
+                   f"timed once with {threads} threads ({t_all:.2f} s) and "
+                   f"once with 1 thread ({t_one:.2f} s)"),
     }
 
 
@@ -267,12 +287,10 @@ def run_reference(args, rank, world):
     from ancestral_draft_sampling_gb300 import workloads as wl
     w = wl.make_config(CONFIG_ID)
     threads = cpu_threads()
-    n = min(w.B, threads)
     for _ in range(args.warmup):
-        oracle_block_seconds(w, n, threads)
-    times = [oracle_block_seconds(w, n, threads) for _ in range(args.steps)]
-    waves = -(-w.B // threads)
-    us = statistics.mean(times) * waves * 1e6
+        oracle_block_seconds(w, threads)
+    times = [oracle_block_seconds(w, threads) for _ in range(args.steps)]
+    us = statistics.mean(times) * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": "us",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -281,9 +299,9 @@ def run_reference(args, rank, world):
         "config": workload_desc(w),
         "cpu_baseline": {"value": us, "unit": "us", "cores": threads,
                          "kind": "oracle",
-                         "sample": (f"each step: {n} of {w.B} requests x {w.K} "
-                                    f"positions in one parallel wave, scaled "
-                                    f"by {waves} waves")},
+                         "sample": (f"each step: the whole block ({w.B} "
+                                    f"requests x {w.K} positions) with "
+                                    f"{threads} threads")},
         "e2e": {"value": us, "unit": "us", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -292,6 +310,151 @@ def run_reference(args, rank, world):
 
 
 # ------------------------------------------------------------- GPU arm
+class GraphBlock:
+    """One workload on the device with its outputs, its workspace and the
+    draft block captured into a CUDA graph on a side stream."""
+
+    def __init__(self, w, device):
+        import torch
+
+        import ancestral_draft_sampling_gb300 as pkg
+        from ancestral_draft_sampling_gb300 import workloads as wl
+        self.w = w
+        self.dev = wl.to_device(w, device)
+        B, K, V, r = w.B, w.K, w.V, w.r
+        self.tokens = torch.empty((B, K), dtype=torch.int32, device=device)
+        self.logits = torch.empty((B, K, V), dtype=torch.float32, device=device)
+        self.probs = torch.empty((B, K, V), dtype=torch.float32, device=device)
+        self.ws = pkg.DraftWorkspace(B, K, V, r, device=device)
+        self.side = torch.cuda.Stream()
+        self.side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(self.side):
+            self.call(self.side)
+        torch.cuda.synchronize()
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph, stream=self.side):
+            self.call(self.side)
+        torch.cuda.synchronize()
+
+    def kwargs(self):
+        d = self.dev
+        return dict(greedy=d["greedy"], pad_row=d["pad_row"], tokens=self.tokens,
+                    logits=self.logits, draft_probs=self.probs,
+                    workspace=self.ws)
+
+    def args(self):
+        d = self.dev
+        return (d["base"], d["U"], d["Wb"], d["d0"], d["seed"], d["offset"],
+                self.w.T)
+
+    def call(self, stream=None):
+        import ancestral_draft_sampling_gb300 as pkg
+        pkg.draft_block(*self.args(), stream=stream, **self.kwargs())
+
+    def time_replays(self, n):
+        """Milliseconds of n back-to-back graph replays (CUDA events on the
+        current stream)."""
+        import torch
+        cur = torch.cuda.current_stream()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        for _ in range(n):
+            self.graph.replay()
+        e1.record(cur)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
+    def timeline(self, replays):
+        """(position chain ms, proposal writer ms) in the block's own
+        schedule: dspark_draft_block_timeline's graph with event nodes."""
+        import ancestral_draft_sampling_gb300 as pkg
+        return pkg.draft_block_timeline(*self.args(), replays=replays,
+                                        stream=self.side, **self.kwargs())
+
+    def profile(self, reps):
+        """Per-launch event brackets (dspark_draft_block_profile), summed
+        over reps blocks: {class: [ms, launches]}."""
+        import ancestral_draft_sampling_gb300 as pkg
+        prof = {"position": [0.0, 0], "pick": [0.0, 0], "proposal": [0.0, 0]}
+        for _ in range(reps):
+            p = pkg.draft_block_profile(*self.args(), **self.kwargs())
+            for key, (ms, n) in p.items():
+                prof[key][0] += ms
+                prof[key][1] += n
+        return prof
+
+
+def position_roofline(w, chain_ms, peak):
+    """The position kernel in the block's schedule: the chain's time (the
+    memset, K positions and the last pick) over K launches."""
+    per_launch_ms = chain_ms / w.K
+    alg = position_kernel_bytes(w)
+    achieved = alg / (per_launch_ms * 1e-3) / 1e9
+    return per_launch_ms, achieved, achieved / peak
+
+
+def measure_config(cfg, steps, peak, device):
+    """µs per block of configuration cfg from graph replays, its fraction of
+    the compulsory-byte floor, and the position kernel's fraction."""
+    import torch
+
+    import ancestral_draft_sampling_gb300 as pkg
+    from ancestral_draft_sampling_gb300 import workloads as wl
+    w = wl.make_config(cfg)
+    gb = GraphBlock(w, device)
+    for _ in range(3):
+        gb.graph.replay()
+    torch.cuda.synchronize()
+    n = max(20, steps)
+    us = gb.time_replays(n) / n * 1e3
+    chain_ms, prop_ms = gb.timeline(10)
+    per_launch_ms, pos_gbs, pos_frac = position_roofline(w, chain_ms, peak)
+    comp = compulsory_bytes(w)
+    out = {
+        "workload": (f"B={w.B} K={w.K} V={w.V} r={w.r}, "
+                     f"{'f32' if w.base_dtype == 0 else 'bf16'} drafter logits, "
+                     f"bf16 head, T={w.T}"
+                     + (", 4 greedy rows" if w.greedy is not None else "")),
+        "us_per_block": us, "replays": n,
+        "compulsory_bytes": comp,
+        "floor_us": comp / (peak * 1e9) * 1e6,
+        "block_hbm_frac": comp / (us * 1e-6) / 1e9 / peak,
+        "position": {"us_per_launch_in_chain": per_launch_ms * 1e3,
+                     "alg_bytes_per_launch": position_kernel_bytes(w),
+                     "achieved_gbs": pos_gbs, "frac": pos_frac},
+        "proposal_us": prop_ms * 1e3,
+    }
+    if w.target is not None:
+        # the configuration as configured: the drafts verified against its
+        # target probabilities by both rules
+        gb.graph.replay()
+        torch.cuda.synchronize()
+        rules = {}
+        for name, fn in (("standard", pkg.verify_standard),
+                         ("block", pkg.verify_block)):
+            acc = torch.empty(w.B, dtype=torch.int32, device=device)
+            emit = torch.empty(w.B, dtype=torch.int32, device=device)
+            args = (gb.probs, gb.dev["target"], gb.tokens, gb.dev["seed"],
+                    gb.dev["offset"])
+            for _ in range(3):
+                fn(*args, accepted_len=acc, emitted_token=emit)
+            cur = torch.cuda.current_stream()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            for _ in range(20):
+                fn(*args, accepted_len=acc, emitted_token=emit)
+            e1.record(cur)
+            torch.cuda.synchronize()
+            rules[name] = {"us_per_call": e0.elapsed_time(e1) / 20 * 1e3,
+                           "mean_accepted_len": float(acc.float().mean())}
+        out["verify"] = rules
+    del gb
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -300,10 +463,10 @@ def run_ours(args, rank, world):
     __graft_entry__.build_library()
     import ancestral_draft_sampling_gb300 as pkg
     from ancestral_draft_sampling_gb300 import workloads as wl
-    from tests.parity import to_device
 
     local = _env_int("LOCAL_RANK", 0)
     torch.cuda.set_device(local)
+    device = f"cuda:{local}"
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -313,87 +476,76 @@ def run_ours(args, rank, world):
     if args.positions != w.K:
         w.K = args.positions
         w.base = np.ascontiguousarray(w.base[:, :w.K])
-    dev = to_device(w, f"cuda:{local}")
     B, K, V, r = w.B, w.K, w.V, w.r
-    tokens = torch.empty((B, K), dtype=torch.int32, device="cuda")
-    logits = torch.empty((B, K, V), dtype=torch.float32, device="cuda")
-    probs = torch.empty((B, K, V), dtype=torch.float32, device="cuda")
-    ws = pkg.DraftWorkspace(B, K, V, r)
-
-    def call(stream=None):
-        pkg.draft_block(dev["base"], dev["U"], dev["Wb"], dev["d0"], dev["seed"],
-                        dev["offset"], w.T, greedy=dev["greedy"],
-                        pad_row=dev["pad_row"], tokens=tokens, logits=logits,
-                        draft_probs=probs, workspace=ws, stream=stream)
 
     if args.mode == "ncu":
+        dev = wl.to_device(w, device)
         for _ in range(args.blocks):
-            call()
+            pkg.draft_block(dev["base"], dev["U"], dev["Wb"], dev["d0"],
+                            dev["seed"], dev["offset"], w.T,
+                            greedy=dev["greedy"], pad_row=dev["pad_row"])
         torch.cuda.synchronize()
         return 0
 
-    side = torch.cuda.Stream()
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        call(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=side):
-        call(side)
-    torch.cuda.synchronize()
-
+    gb = GraphBlock(w, device)
+    dev = gb.dev
     for _ in range(args.warmup):
-        graph.replay()
+        gb.graph.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     cur = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clocks:
+    with ClockSampler(nvsmi_gpu_id(local)) as clocks:
         torch.cuda.synchronize()
         clocks.start()
         ev0.record(cur)
         for _ in range(args.steps):
-            graph.replay()
+            gb.graph.replay()
         ev1.record(cur)
+        # the clock window: the same replays continue (no gap) for about a
+        # second, so that the clock record holds many samples; its own time
+        # is reported beside the timed region's
+        cw_steps = max(args.steps, int(1.0 / 0.00048))
+        ev2 = torch.cuda.Event(enable_timing=True)
+        for _ in range(cw_steps):
+            gb.graph.replay()
+        ev2.record(cur)
         torch.cuda.synchronize()
         clocks.stop()
     ms_step, us_per_block = job_timing(ev0.elapsed_time(ev1), args.steps,
                                        world, dist, "cuda")
-
-    # per-kernel durations, CUDA events around every launch on its stream
-    prof = {"position": [0.0, 0], "pick": [0.0, 0], "proposal": [0.0, 0]}
-    prof_reps = max(3, min(args.steps, 10))
-    for _ in range(prof_reps):
-        p = pkg.draft_block_profile(dev["base"], dev["U"], dev["Wb"], dev["d0"],
-                                    dev["seed"], dev["offset"], w.T,
-                                    greedy=dev["greedy"], pad_row=dev["pad_row"],
-                                    tokens=tokens, logits=logits,
-                                    draft_probs=probs, workspace=ws)
-        for key, (ms, n) in p.items():
-            prof[key][0] += ms
-            prof[key][1] += n
-    dominant = max(prof, key=lambda k: prof[k][0])
-    avg_ms = {k: (v[0] / v[1] if v[1] else 0.0) for k, v in prof.items()}
+    clock_window_us = ev1.elapsed_time(ev2) / cw_steps * 1e3
     peak, peak_kind = measured_peaks()
-    if dominant == "position":
-        alg_bytes = position_kernel_bytes(w)
-    elif dominant == "proposal":
-        alg_bytes = 2 * B * K * V * 4
-    else:  # the pick reads one 16-byte statistic per (request, CTA)
-        n_ctas = min((V + 127) // 128,
-                     torch.cuda.get_device_properties(0).multi_processor_count)
-        alg_bytes = B * n_ctas * 16
-    achieved = alg_bytes / (avg_ms[dominant] * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dominant, "achieved": achieved,
-                "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                "frac": achieved / peak,
-                "traffic": ncu_traffic(dominant),
-                "alg_bytes_per_launch": alg_bytes,
-                "avg_launch_ms": avg_ms[dominant],
-                "stage_avg_ms": avg_ms,
-                "stage_share": {k: v[0] / sum(x[0] for x in prof.values())
-                                for k, v in prof.items()}}
+
+    # the position kernel in the block's own schedule (graph replay, the
+    # positions chained by programmatic dependent launch)
+    chain_ms, prop_ms = gb.timeline(max(5, min(args.steps, 20)))
+    per_launch_ms, achieved, frac = position_roofline(w, chain_ms, peak)
+    # every launch bracketed by events (no overlap between launches)
+    prof_reps = max(3, min(args.steps, 10))
+    prof = gb.profile(prof_reps)
+    iso_ms = {k: (v[0] / v[1] if v[1] else 0.0) for k, v in prof.items()}
+    iso_gbs = position_kernel_bytes(w) / (iso_ms["position"] * 1e-3) / 1e9
+    roofline = {
+        "bound": "hbm", "kernel": "position_tc_kernel",
+        "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+        "unit": "GB/s", "frac": frac,
+        "traffic": ncu_traffic("position"),
+        "alg_bytes_per_launch": position_kernel_bytes(w),
+        "avg_launch_ms": per_launch_ms,
+        "schedule": ("graph replay of the block, positions chained by "
+                     "programmatic dependent launch; avg launch = (event "
+                     "node before the memset .. event node after the last "
+                     "pick) / K, so the memset and the pick are counted "
+                     "against the position kernel (dspark_draft_block_timeline)"),
+        "isolated": {
+            "schedule": ("every launch bracketed by CUDA events, no overlap "
+                         "between launches (dspark_draft_block_profile)"),
+            "avg_launch_ms": iso_ms, "position_frac": iso_gbs / peak,
+            "launches_per_block": {k: v[1] // prof_reps for k, v in prof.items()}},
+        "proposal_ms_in_graph": prop_ms,
+    }
     block_gbs = compulsory_bytes(w) / (ms_step * 1e-3) / 1e9
 
     # end to end through the public API with host buffers
@@ -407,7 +559,6 @@ def run_ours(args, rank, world):
             host_small[k2] = dev[k2].cpu().pin_memory()
     host_tokens = torch.empty((B, K), dtype=torch.int32).pin_memory()
     e2e_steps = max(3, min(args.steps, 10))
-    cur = torch.cuda.current_stream()
     copy_stream = torch.cuda.Stream()
     host_ws = pkg.HostWorkspace(B, K, V, r)
 
@@ -416,8 +567,8 @@ def run_ours(args, rank, world):
         # on copy_stream while earlier positions compute; tokens copied back
         pkg.draft_block_host(host_base, dev["U"], dev["Wb"], host_small["d0"],
                              host_small["seed"], host_small["offset"], w.T,
-                             base_dev=dev["base"], logits=logits,
-                             draft_probs=probs, tokens_host=host_tokens,
+                             base_dev=dev["base"], logits=gb.logits,
+                             draft_probs=gb.probs, tokens_host=host_tokens,
                              greedy_host=host_small.get("greedy"),
                              pad_row_host=host_small.get("pad_row"),
                              workspace=host_ws, stream=cur,
@@ -436,25 +587,26 @@ def run_ours(args, rank, world):
         t.numel() * t.element_size() for t in host_small.values())
     d2h = host_tokens.numel() * 4
     # the last call's tokens came back through host memory
-    assert torch.equal(host_tokens, tokens.cpu()), "host-fed tokens differ"
+    assert torch.equal(host_tokens, gb.tokens.cpu()), "host-fed tokens differ"
+    del host_base
 
     # secondary path: standard verification of this block's drafts against
     # target distributions softmax(l + N(0,1)) (timing inputs, made by torch)
-    gen = torch.Generator(device="cuda")
+    gen = torch.Generator(device=device)
     gen.manual_seed(5)
-    tl = torch.cat([logits, logits[:, -1:]], dim=1)
-    tl = tl + torch.randn(tl.shape, device="cuda", generator=gen)
+    tl = torch.cat([gb.logits, gb.logits[:, -1:]], dim=1)
+    tl = tl + torch.randn(tl.shape, device=device, generator=gen)
     target = torch.softmax(tl.nan_to_num(neginf=-1e30), dim=-1)
     # temperature-only target sampling of the same B x (K+1) target rows
     tl_rows = tl.reshape(B * (K + 1), V).contiguous()
     del tl
     seed_rows = dev["seed"].repeat_interleave(K + 1)
     off_rows = dev["offset"].repeat_interleave(K + 1)
-    pos_rows = torch.arange(K + 1, dtype=torch.int32, device="cuda").repeat(B)
-    smp_tok = torch.empty(B * (K + 1), dtype=torch.int32, device="cuda")
+    pos_rows = torch.arange(K + 1, dtype=torch.int32, device=device).repeat(B)
+    smp_tok = torch.empty(B * (K + 1), dtype=torch.int32, device=device)
     smp_probs = torch.empty_like(tl_rows)
     smp_ws = torch.empty(pkg._lib.load().dspark_sample_workspace_bytes(B * (K + 1), V),
-                         dtype=torch.uint8, device="cuda")
+                         dtype=torch.uint8, device=device)
 
     def sample_call():
         pkg.sample_temperature(tl_rows, seed_rows, off_rows, T=1.0,
@@ -476,20 +628,21 @@ def run_ours(args, rank, world):
                "bytes": 3 * B * (K + 1) * V * 4,
                "note": "temperature-only sampling of the block's target rows "
                        "(token and probabilities per row)"}
+    sampler["hbm_frac"] = sampler["bytes"] / (sampler["us_per_call"] * 1e-6) / 1e9 / peak
     del tl_rows, smp_probs
-    acc_len = torch.empty(B, dtype=torch.int32, device="cuda")
-    emitted = torch.empty(B, dtype=torch.int32, device="cuda")
+    acc_len = torch.empty(B, dtype=torch.int32, device=device)
+    emitted = torch.empty(B, dtype=torch.int32, device=device)
 
     def time_rule(fn, n_ver=20):
         for _ in range(3):
-            fn(probs, target, tokens, dev["seed"], dev["offset"],
+            fn(gb.probs, target, gb.tokens, dev["seed"], dev["offset"],
                accepted_len=acc_len, emitted_token=emitted)
         torch.cuda.synchronize()
         f0 = torch.cuda.Event(enable_timing=True)
         f1 = torch.cuda.Event(enable_timing=True)
         f0.record(cur)
         for _ in range(n_ver):
-            fn(probs, target, tokens, dev["seed"], dev["offset"],
+            fn(gb.probs, target, gb.tokens, dev["seed"], dev["offset"],
                accepted_len=acc_len, emitted_token=emitted)
         f1.record(cur)
         torch.cuda.synchronize()
@@ -506,9 +659,25 @@ def run_ours(args, rank, world):
                         "bytes": 2 * B * (K - 1) * V * 4 + B * V * 8,
                         "note": "block verification of the same drafts: reads "
                                 "the K-1 rows p_1..p_{K-1}, q_1..q_{K-1} in full"}}
+    verify["block"]["hbm_frac"] = (verify["block"]["bytes"] /
+                                   (block_us * 1e-6) / 1e9 / peak)
     del target
 
+    per_config = None
+    if world == 1 and not args.no_per_config:
+        del gb
+        torch.cuda.empty_cache()
+        per_config = {str(c): measure_config(c, args.steps, peak, device)
+                      for c in (2, 3, 5)}
+
     if rank == 0:
+        clock = clocks.summary()
+        clock["gpu"] = nvsmi_gpu_id(local)
+        clock["window_note"] = (
+            f"samples from the timed region and the clock window that follows "
+            f"it without a gap ({cw_steps} more replays, "
+            f"{clock_window_us:.1f} us per block)")
+        launches_per_block = sum(v[1] for v in prof.values()) // prof_reps
         line = {
             "metric": METRIC, "value": us_per_block, "unit": "us",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -521,11 +690,11 @@ def run_ours(args, rank, world):
             "block_hbm_frac": block_gbs / peak,
             "compulsory_bytes_per_block": compulsory_bytes(w),
             "roofline": roofline,
-            "clocks": clocks.summary(),
+            "clocks": clock,
             "verify": verify,
             "target_sampler": sampler,
             # kernels of one block (counted by the profile pass) x steps
-            "gpu_launches": args.steps * sum(v[1] for v in prof.values()) // prof_reps,
+            "gpu_launches": args.steps * launches_per_block,
             "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h,
                     "path": "dspark_draft_block_host: pinned-host drafter "
@@ -533,6 +702,8 @@ def run_ours(args, rank, world):
                             "overlapped with the kernels; tokens copied back "
                             "to pinned host memory"},
         }
+        if per_config is not None:
+            line["per_config"] = per_config
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(w)
         print(json.dumps(line), flush=True)
@@ -548,6 +719,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the B = 8, 44, 64 configurations")
     ap.add_argument("--mode", choices=["bench", "ncu"], default="bench",
                     help="ncu: run a few eager blocks and exit (a small, "
                          "self-ending workload for profiler captures)")

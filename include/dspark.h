@@ -27,9 +27,13 @@
  * Conventions for every entry point:
  *   - All tensors are dense, row-major, and live in device memory unless
  *     stated otherwise.  The caller owns every buffer; the library does not
- *     allocate, free, synchronise, print or trap.
- *   - Calls are asynchronous on `stream` and may be captured in a CUDA graph
- *     (all launches are plain kernel launches on `stream`).
+ *     allocate, free, print or trap, and does not synchronise except in the
+ *     calls documented as synchronising (the measurement variants
+ *     dspark_draft_block_profile and dspark_draft_block_timeline, and
+ *     dspark_read_device_error).
+ *   - Calls are asynchronous on `stream` and, except those three, may be
+ *     captured in a CUDA graph (their work is kernel launches and memsets on
+ *     `stream`).
  *   - Argument checks run on the host before any launch; a failing check
  *     returns a status and enqueues nothing.  A launch failure returns
  *     DSPARK_ERR_CUDA (from cudaGetLastError).
@@ -78,12 +82,14 @@ typedef enum {
 
 /*
  * Bytes of device workspace dspark_draft_block needs for these sizes
- * (0 if the sizes are unsupported).  The workspace holds per-chunk softmax
- * statistics (two buffers, so consecutive positions do not overwrite each
- * other's), per-row (max, sum-exp) of every position, the decision keys the
- * position kernels share across CTAs, and a device error word.  Its
- * contents need not be initialised and are overwritten by each call; two
- * calls in flight at the same time must not share a workspace.
+ * (0 if the sizes are unsupported).  The workspace holds a device error
+ * word (its first 4 bytes), the decision keys the position kernels share
+ * across CTAs, per-chunk softmax statistics (two buffers, so consecutive
+ * positions do not overwrite each other's) and per-row (max, sum-exp) of
+ * every position.  Its contents need not be initialised: every call first
+ * clears the error word and the keys (one 2-D memset on `stream`), and
+ * every other word is written before it is read.  Two calls in flight at
+ * the same time must not share a workspace.
  */
 DSPARK_API size_t dspark_draft_workspace_bytes(int B, int K, int V, int r);
 
@@ -147,6 +153,31 @@ DSPARK_API dspark_status dspark_draft_block_profile(
     cudaStream_t stream);
 
 /*
+ * dspark_draft_block_timeline -- measurement variant of dspark_draft_block
+ * that keeps the block's own schedule (positions chained by programmatic
+ * dependent launch, no event between them).  It captures one
+ * dspark_draft_block launch sequence from `stream` into a CUDA graph, with
+ * event nodes at its start, between the position chain (the memset, the K
+ * position kernels and their picks) and the proposal writer, and at its
+ * end; it then replays the graph `replays` (>= 1) times, synchronising
+ * after each replay, and returns the mean duration of each segment:
+ *   chain_ms[1], proposal_ms[1] (host) -- milliseconds per replay.
+ * `stream` must be a created stream (not the legacy NULL stream; status
+ * DSPARK_ERR_INVALID_ARG) that is not already capturing.  Outputs are
+ * identical to dspark_draft_block's.  It creates three events, a graph and
+ * its executable (the driver allocates for them) and destroys them before
+ * returning; it synchronises and must not itself be captured.
+ */
+DSPARK_API dspark_status dspark_draft_block_timeline(
+    const void* base_logits, dspark_dtype base_dtype, const void* U,
+    const void* Wb, dspark_dtype w_dtype, const int32_t* d0,
+    const uint64_t* seed, const uint64_t* offset, float T,
+    const uint8_t* greedy, const uint8_t* pad_row, int B, int K, int V, int r,
+    int32_t* tokens, float* logits, float* draft_probs, void* workspace,
+    size_t workspace_bytes, int replays, float* chain_ms, float* proposal_ms,
+    cudaStream_t stream);
+
+/*
  * dspark_draft_block_per_request -- dspark_draft_block with a temperature
  * per request and slot-indexed proposals, as a serving batch needs them
  * (PR #27, "2. One fused kernel per draft position": the proposal writer
@@ -193,14 +224,17 @@ DSPARK_API dspark_status dspark_draft_block_per_request(
  * array of DSPARK_NOALLOC_SCRATCH_BYTES bytes (2 MiB), held on every GPU
  * that loads the library until the process exits; sizes whose workspace
  * (dspark_draft_workspace_bytes) exceeds it are rejected with
- * DSPARK_ERR_WORKSPACE before any launch (B <= 102 fits at K = 7).
+ * DSPARK_ERR_WORKSPACE before any launch (B <= 101 fits at K = 7).
  * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
- * routine.  The first call on a device looks up the scratch's device
- * address (with that device current); make that first call before any
- * stream capture.  Every call on a device shares the one scratch array and
- * it keeps the last call's contents (each call zeroes the device error word
- * it starts with); calls that overlap on the GPU, from any stream or thread,
- * race on it and must be serialised by the caller.  Device-side error codes
+ * routine.  Each call made outside stream capture looks up the scratch's
+ * device address on the current device (so a device reset or a new primary
+ * context is followed); a call made during a capture uses the address the
+ * last uncaptured call on that device found, so the first call on a device
+ * must come before any capture, and a capture must not outlive a device
+ * reset.  Every call on a device shares the one scratch array and it keeps
+ * the last call's contents (each call clears the device error word and the
+ * decision keys it starts with); calls that overlap on the GPU, from any
+ * stream or thread, race on it and must be serialised by the caller.  Device-side error codes
  * of this variant stay in the scratch and are not reported.
  */
 #define DSPARK_NOALLOC_SCRATCH_BYTES (2u << 20)
@@ -363,10 +397,30 @@ DSPARK_API dspark_status dspark_noise_words(uint64_t seed, uint64_t offset, int 
                                  float* gumbel, cudaStream_t stream);
 
 /*
+ * dspark_noise_words_folded -- the same diagnostic computed the way the
+ * position, verification and sampler kernels compute their noise: the parts
+ * of Philox4x32-10's first two rounds that depend only on the key and the
+ * fixed counter words (k | stream << 16, offset lo, offset hi) are folded
+ * into per-request constants, and the round keys are precomputed.  Its
+ * words must equal dspark_noise_words' (and the published Philox4x32-10's)
+ * bit for bit; arguments and errors are those of dspark_noise_words.
+ */
+DSPARK_API dspark_status dspark_noise_words_folded(uint64_t seed, uint64_t offset,
+                                        int k, int stream_id, int n,
+                                        uint32_t* out, float* gumbel,
+                                        cudaStream_t stream);
+
+/*
  * dspark_read_device_error -- copies the device error word of `workspace`
  * to the host (synchronising `stream`) and clears it.  Returns DSPARK_OK if
- * no kernel recorded an error, DSPARK_ERR_DEVICE (and *code != 0) if one
- * did.  This is the only call that synchronises.
+ * no kernel of the last call on this workspace recorded an error,
+ * DSPARK_ERR_DEVICE (and *code != 0) if one did.  Every draft-block and
+ * sampler call clears the word when it starts, so the code describes the
+ * last call only.  Codes: 1 a d0 outside [0, V) (token 0 used), 2 a bounded
+ * wait inside a kernel ran out, 3 a per-request temperature that is not
+ * finite and positive (1 used), 4 a proposal slot outside [0, num_slots),
+ * 5 a sampler position outside [0, 65535] (0 used).  Synchronises
+ * `stream`.
  */
 DSPARK_API dspark_status dspark_read_device_error(void* workspace, int* code,
                                        cudaStream_t stream);

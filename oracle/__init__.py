@@ -66,6 +66,8 @@ def _load():
         lib.oracle_philox4x32_10.restype = None
         lib.oracle_noise_word.argtypes = [U64, U64, I, I, ctypes.c_uint32]
         lib.oracle_noise_word.restype = ctypes.c_uint32
+        lib.oracle_noise_words.argtypes = [U64, U64, I, I, ctypes.c_uint32, P]
+        lib.oracle_noise_words.restype = None
         lib.oracle_gumbel.argtypes = [ctypes.c_uint32]
         lib.oracle_gumbel.restype = ctypes.c_double
         lib.oracle_accept_uniform.argtypes = [ctypes.c_uint32]
@@ -113,6 +115,13 @@ def philox4x32_10(ctr, key) -> np.ndarray:
 
 def noise_word(seed: int, offset: int, k: int, stream: int, index: int) -> int:
     return int(_load().oracle_noise_word(seed, offset, k, stream, index))
+
+
+def noise_words(seed: int, offset: int, k: int, stream: int, n: int) -> np.ndarray:
+    """Words of elements 0 .. n-1: ``noise_word`` for each index."""
+    out = np.empty(n, dtype=np.uint32)
+    _load().oracle_noise_words(seed, offset, k, stream, n, _ptr(out))
+    return out
 
 
 def gumbel(x: int) -> float:

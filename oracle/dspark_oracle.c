@@ -105,6 +105,14 @@ uint32_t oracle_noise_word(uint64_t seed, uint64_t offset, int k, int stream,
   return out[index & 3u];
 }
 
+/* The words of elements 0 .. n-1 (oracle_noise_word for each index), for
+ * comparisons over long stretches of counters. */
+void oracle_noise_words(uint64_t seed, uint64_t offset, int k, int stream,
+                        uint32_t n, uint32_t* out) {
+  for (uint32_t i = 0; i < n; ++i)
+    out[i] = oracle_noise_word(seed, offset, k, stream, i);
+}
+
 /* Standard Gumbel variate from one 32-bit word: w uniform in (0, 1),
  * g = -log(-log(1 - w)). */
 double oracle_gumbel(uint32_t x) {

@@ -138,6 +138,49 @@ def test_noise_words_rejects_bad_arguments(lib):
     assert f(1, 2, 0, 0, 16, FAKE + 4, None, None) == INVALID
 
 
+def test_noise_words_folded_rejects_bad_arguments(lib):
+    f = lib.dspark_noise_words_folded
+    assert f(1, 2, 0, 0, 0, FAKE, None, None) == INVALID
+    assert f(1, 2, 0, 0, 16, None, None, None) == INVALID
+    assert f(1, 2, 0x10000, 0, 16, FAKE, None, None) == INVALID
+    assert f(1, 2, 0, 0, 16, FAKE, FAKE + 8, None) == INVALID
+
+
+def _timeline_call(lib, a, replays=3, chain=True, prop=True, stream=1):
+    import ctypes
+    c, p = ctypes.c_float(0), ctypes.c_float(0)
+    return lib.dspark_draft_block_timeline(
+        a["base"], a["base_dtype"], a["U"], a["Wb"], a["w_dtype"], a["d0"],
+        a["seed"], a["offset"], a["T"], a["greedy"], a["pad_row"], a["B"],
+        a["K"], a["V"], a["r"], a["tokens"], a["logits"], a["probs"],
+        a["workspace"], a["ws_bytes"], replays,
+        ctypes.byref(c) if chain else None, ctypes.byref(p) if prop else None,
+        stream)
+
+
+@pytest.mark.parametrize("kw,over,want", [
+    (dict(stream=None), {}, INVALID),       # the legacy stream cannot capture
+    (dict(replays=0), {}, INVALID),
+    (dict(chain=False), {}, INVALID),
+    (dict(prop=False), {}, INVALID),
+    (dict(), dict(T=0.0), INVALID),         # the block's own checks
+    (dict(), dict(r=40), UNSUPPORTED),
+    (dict(), dict(ws_bytes=100), WORKSPACE),
+])
+def test_draft_block_timeline_rejects_bad_arguments(lib, kw, over, want):
+    assert _timeline_call(lib, _draft_args(lib, **over), **kw) == want
+
+
+def test_workspace_starts_with_the_error_word_row(lib):
+    """The error word sits at offset 0 and the decision-key rows follow it
+    at a 4 KB pitch, so one 2-D memset clears both: the workspace grows by
+    one 4 KB row per request plus one for the error word."""
+    ws = lib.dspark_draft_workspace_bytes
+    per_request = ws(9, 7, 200064, 256) - ws(8, 7, 200064, 256)
+    assert per_request >= 4096 + 2 * 512 * 16
+    assert ws(1, 1, 16, 16) >= 2 * 4096
+
+
 def test_read_device_error_rejects_null(lib):
     import ctypes
     code = ctypes.c_int(0)

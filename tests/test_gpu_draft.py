@@ -56,6 +56,26 @@ def test_gumbel_tails_bit_for_word():
         assert abs(g[i] - oracle.gumbel(int(words[i]))) <= 4 * 2.0**-19
 
 
+@pytest.mark.parametrize("seed,offset,k,stream", [
+    (0, 0, 0, 0), (2**64 - 1, 2**64 - 1, 0xFFFF, 3), (2**32 - 1, 2**32, 6, 0),
+    (2**32, 2**32 - 1, 3, 1), (0x9E3779B97F4A7C15, 12345, 1, 2)])
+def test_folded_noise_words_bit_exact_over_a_million_counters(seed, offset, k,
+                                                              stream):
+    """The folded Philox the position, verification and sampler kernels run
+    (rounds 1-2 folded into per-request constants) gives the published
+    Philox4x32-10 words bit for bit: 2^20 words (262,144 counters) per
+    (seed, offset, position, stream), 1.3 M counters over the five cases,
+    with the extremes of seed, offset and the counter's position word."""
+    n = 1 << 20
+    words, g = pkg.noise_words(seed, offset, k, stream, n, folded=True)
+    words = words.cpu().numpy().view(np.uint32)
+    ref = oracle.noise_words(seed, offset, k, stream, n)
+    np.testing.assert_array_equal(words, ref)
+    plain, gp = pkg.noise_words(seed, offset, k, stream, n)
+    np.testing.assert_array_equal(plain.cpu().numpy().view(np.uint32), ref)
+    np.testing.assert_array_equal(g.cpu().numpy(), gp.cpu().numpy())
+
+
 # ------------------------------------------------------- small-shape parity
 SMALL_CASES = [
     # B, K, V, r, base dtype, w dtype, T, extra
@@ -277,20 +297,46 @@ def test_draws_follow_softmax_and_condition_on_previous(bdt):
         assert _chi2(toks[m, 1], p1) > 1e-4
 
 
-# ------------------------------------------------------- full-size configs
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_full_config_sampled_parity(cfg):
-    w = wl.make_config(cfg)
-    tokens, logits, probs = _np(run_draft(w))
-    rows = default_rows(w.B, w.K, max_rows=max(w.B, 96), seed=cfg)
-    st = check_block_against_oracle(w, tokens, logits, probs, rows=rows)
-    assert st["near_tie_token_diffs"] <= 1
-    # properties that hold at any size, on every row
-    assert ((tokens >= 0) & (tokens < w.V)).all()
-    sums = probs.astype(np.float64).sum(-1)
-    np.testing.assert_allclose(sums, 1.0, rtol=0, atol=1e-4)
-    assert np.isfinite(probs).all()
-    if w.greedy is not None:
-        g = np.flatnonzero(w.greedy)
-        s = logits[g] / np.float32(w.T)
-        np.testing.assert_array_equal(tokens[g], s.argmax(-1))
+@pytest.mark.parametrize("V", [128, 384])
+@pytest.mark.parametrize("bdt", [wl.F32, wl.BF16])
+def test_tensor_core_draws_follow_softmax_and_condition_on_previous(V, bdt,
+                                                                     monkeypatch):
+    """The same chi-square tests (p = 1e-4) on the tensor-core kernel itself
+    (bf16 head, r = 64): one vocab chunk (V = 128, one CTA) and three
+    (V = 384, three CTAs whose winners meet through the decision keys), with
+    f32 and bf16 drafter logits; position 0 against softmax(l0 / T) and
+    position 1 given each of the three likeliest position-0 tokens."""
+    monkeypatch.setenv("DSPARK_POSITION_KERNEL", "tc")  # fail if not taken
+    r, K, T = 64, 2, 0.9
+    B, calls = 96, 1300
+    rng = np.random.Generator(np.random.PCG64(int(bdt) + 11 + V))
+    base_rows = (rng.standard_normal((K, V)) * 0.6).astype(np.float32)
+    base_rows[:, :6] += 3.0
+    U_bits = wl.to_bf16_bits((rng.standard_normal((V, r)) * 0.4).astype(np.float32))
+    Wb_bits = wl.to_bf16_bits((rng.standard_normal((r, V)) * 0.4).astype(np.float32))
+    if bdt == wl.BF16:
+        base_np = wl.to_bf16_bits(np.broadcast_to(base_rows, (B, K, V)).copy())
+        base_f = wl.bf16_bits_to_f32(base_np[0])
+    else:
+        base_np = np.broadcast_to(base_rows, (B, K, V)).copy()
+        base_f = base_rows
+    w = wl.Workload("chi2_tc", B, K, V, r, T, base_np, U_bits, Wb_bits,
+                    np.full(B, 5, np.int32), np.zeros(B, np.uint64),
+                    np.zeros(B, np.uint64))
+    dev = to_device(w)
+    toks = []
+    for c in range(calls):
+        dev["seed"].copy_(torch.arange(B, dtype=torch.int64) + c * B + 29)
+        toks.append(run_draft(w, dev)[0].cpu().numpy())
+    toks = np.concatenate(toks)
+    U64 = wl.bf16_bits_to_f32(U_bits).astype(np.float64)
+    W64 = wl.bf16_bits_to_f32(Wb_bits).astype(np.float64)
+    l0 = (base_f[0].astype(np.float64) + U64[5] @ W64).astype(np.float32)
+    p0 = special.softmax((l0 / np.float32(T)).astype(np.float64))
+    assert _chi2(toks[:, 0], p0) > 1e-4
+    for a in np.argsort(-p0)[:3]:
+        l1 = (base_f[1].astype(np.float64) + U64[a] @ W64).astype(np.float32)
+        p1 = special.softmax((l1 / np.float32(T)).astype(np.float64))
+        m = toks[:, 0] == a
+        assert m.sum() > 2000
+        assert _chi2(toks[m, 1], p1) > 1e-4

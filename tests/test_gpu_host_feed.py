@@ -10,7 +10,8 @@ import torch
 
 import ancestral_draft_sampling_gb300 as pkg
 from ancestral_draft_sampling_gb300 import workloads as wl
-from tests.parity import _t, run_draft, to_device
+from ancestral_draft_sampling_gb300.workloads import _tensor as _t
+from tests.parity import run_draft, to_device
 
 pytestmark = pytest.mark.gpu
 

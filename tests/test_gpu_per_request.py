@@ -105,7 +105,7 @@ def test_invalid_temperature_counts_as_one_and_is_reported():
     fixed = temps.copy()
     fixed[2] = fixed[4] = fixed[6] = 1.0
     ws = pkg.DraftWorkspace(w.B, w.K, w.V, w.r)
-    pkg.read_device_error(ws)
+    ws.buffer.fill_(0xFF)  # stale contents: each call clears the error word
     got = _per_request(w, dev, bad, workspace=ws)
     assert pkg.read_device_error(ws) == 3
     ref = _per_request(w, dev, fixed, workspace=ws)
@@ -123,7 +123,7 @@ def test_slot_out_of_range_writes_nothing_and_is_reported():
     slot = np.array([2, 9, 0, 1], dtype=np.int32)  # 9 is outside 5 slots
     buf = torch.full((5, w.K, w.V), -1.0, device="cuda")
     ws = pkg.DraftWorkspace(w.B, w.K, w.V, w.r)
-    pkg.read_device_error(ws)
+    ws.buffer.fill_(0xFF)  # stale contents: each call clears the error word
     _, _, got = _per_request(w, dev, temps, slot=slot, draft_probs=buf,
                              workspace=ws)
     assert pkg.read_device_error(ws) == 4

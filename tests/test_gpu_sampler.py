@@ -110,12 +110,14 @@ def test_sampler_reports_bad_temperature_and_position():
     nbytes = pkg._lib.load().dspark_sample_workspace_bytes(R, V)
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     handle = types.SimpleNamespace(buffer=ws)
-    pkg.read_device_error(handle)
+    ws.fill_(0xFF)  # stale contents: each call clears the error word
     temps = np.ones(R, np.float32)
     temps[2] = -3.0
     tok, _ = _gpu(x, s, o, temperature=temps, workspace=ws)
     assert pkg.read_device_error(handle) == 3
+    ws.fill_(0xFF)
     ref, _ = _gpu(x, s, o, temperature=np.ones(R, np.float32), workspace=ws)
+    assert pkg.read_device_error(handle) == 0
     np.testing.assert_array_equal(tok, ref)
     pos = np.zeros(R, np.int32)
     pos[4] = 70000

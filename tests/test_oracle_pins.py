@@ -89,6 +89,23 @@ def test_noise_word_counter_layout():
     assert [oracle.noise_word(7, 9, 3, 0, v) for v in range(8, 12)] == list(blk)
 
 
+@pytest.mark.parametrize("seed,offset,k,stream", [
+    (0, 0, 0, 0), (2**64 - 1, 2**64 - 1, 0xFFFF, 3), (2**32, 2**32 - 1, 6, 1)])
+def test_noise_words_range_is_the_published_philox(seed, offset, k, stream):
+    """The range form (used for long GPU comparisons) gives, for every index
+    v, word v & 3 of Philox4x32-10 at counter (v >> 2, k | stream << 16,
+    offset lo, offset hi) under key (seed lo, seed hi), the function the
+    known answers and cuRAND pin above."""
+    n = 1030  # a ragged last block
+    got = oracle.noise_words(seed, offset, k, stream, n)
+    key = [seed & 0xFFFFFFFF, seed >> 32]
+    c1 = k | (stream << 16)
+    want = np.concatenate([
+        oracle.philox4x32_10([i, c1, offset & 0xFFFFFFFF, offset >> 32], key)
+        for i in range((n + 3) // 4)])[:n]
+    np.testing.assert_array_equal(got, want)
+
+
 def test_gumbel_cdf_and_tails():
     """g(x) for x uniform over 32-bit words follows the standard Gumbel law
     P(g <= t) = exp(-exp(-t)); g decreases in x; the upper tail behaves like
