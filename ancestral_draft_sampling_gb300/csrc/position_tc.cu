@@ -114,8 +114,8 @@ struct TcParams {
   int bpad;
   int stages;
   int tiles_total;
-  int stall_first_wait;  // failure-path test: the MMA issuer's first wait is
-                         // on a phase nothing completes, with a short limit
+  int stall_first_wait;  // failure-path test: the MMA issuer waits for a
+                         // phase nothing completes, with a short limit
   int n_chunks;
   uint32_t u_off, tile_off, stage_off, rows_off, rstate_off, bar_off;
 };
@@ -579,9 +579,12 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16_f32(kTileV, (uint32_t)P.bpad, 1u, 0u);
       const uint32_t u_base = smem_u32(u_s);
-      if (!mbar_wait(u_ready, P.stall_first_wait ? 1u : 0u,
-                     P.stall_first_wait ? kStallPolls : kSpin))
-        fail(kDevErrTimeout);
+      bool u_ok = mbar_wait(u_ready, 0u, kSpin);
+      // failure-path test: once u is ready, a wait for the barrier's second
+      // phase, which nothing completes (u_ready takes one round of arrivals
+      // per launch)
+      if (u_ok && P.stall_first_wait) u_ok = mbar_wait(u_ready, 1u, kStallPolls);
+      if (!u_ok) fail(kDevErrTimeout);
       int g = 0;
       for (int t = 0; t < n_tiles && !*abort_flag; ++t) {
         const int acc = t & 1;
@@ -973,10 +976,11 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
 }
 
 // ------------------------------------------------------------ host side
-// DSPARK_TEST_STALL_WAIT=1 (tests of the failure path only): the MMA
-// issuer's first wait is made on a barrier phase that nothing completes,
-// with a short poll limit, so that it runs out, the kernel records
-// kDevErrTimeout and takes its abort path.  That wait guards no copy.
+// DSPARK_TEST_STALL_WAIT=1 (tests of the failure path only): once u is
+// ready, the MMA issuer waits for the u barrier's second phase, which
+// nothing completes, with a short poll limit, so that the wait runs out,
+// the kernel records kDevErrTimeout and takes its abort path.  That wait
+// guards no copy.
 bool stall_first_wait_requested() {
   const char* env = std::getenv("DSPARK_TEST_STALL_WAIT");
   return env != nullptr && env[0] == '1';
