@@ -113,6 +113,7 @@ struct TcParams {
   int k;
   int bpad;
   int stages;
+  int stage_bufs;  // bf16 drafter-logit staging tiles (1 or 2; 0 for f32)
   int tiles_total;
   int stall_first_wait;  // failure-path test: the MMA issuer waits for a
                          // phase nothing completes, with a short limit
@@ -446,8 +447,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* base_full = acc_empty + 2;
   uint64_t* tile_free = base_full + 2;
-  uint64_t* stage_free = tile_free + 2;
-  uint64_t* mma_done = stage_free + 1;
+  uint64_t* stage_free = tile_free + 2;  // [2]: staging tiles read
+  uint64_t* mma_done = stage_free + 2;
   uint64_t* u_ready = mma_done + 1;
   uint64_t* drained = u_ready + 1;  // [2]: the drain warps have filled a buffer
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drained + 2);
@@ -461,6 +462,12 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   const int n_tiles = (P.tiles_total - 1 - chunk) / P.n_chunks + 1;
   const int kchunks = a.r / kKChunk;
   const int tile_floats = P.bpad * kTileV;
+  // bf16 drafter logits: staging tile and phase of tile t (one or two
+  // staging tiles, see make_layout)
+  auto stage_of = [&](int t) { return P.stage_bufs == 2 ? (t & 1) : 0; };
+  auto stage_parity = [&](int t) {
+    return (uint32_t)(P.stage_bufs == 2 ? (t >> 1) : t) & 1u;
+  };
 
   auto fail = [&](int code) {
     *abort_flag = 1;
@@ -480,7 +487,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       mbar_init(&tile_free[i], kComputeThreads + 1);  // + the storer
       mbar_init(&drained[i], kDrainThreads);
     }
-    mbar_init(stage_free, kDrainThreads);
+    mbar_init(&stage_free[0], kDrainThreads);
+    mbar_init(&stage_free[1], kDrainThreads);
     mbar_init(mma_done, 1);
     mbar_init(u_ready, kWorkThreads);
     *abort_flag = 0;
@@ -556,12 +564,14 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       for (int t = 0; t < n_tiles && !*abort_flag; ++t, ++issued) {
         const int v0 = (chunk + t * P.n_chunks) * kTileV;
         if (kStaged) {
-          if (!mbar_wait(stage_free, ((uint32_t)t & 1u) ^ 1u, kSpin)) {
+          const int sb = stage_of(t);
+          if (!mbar_wait(&stage_free[sb], stage_parity(t) ^ 1u, kSpin)) {
             fail(kDevErrTimeout);
             break;
           }
-          mbar_arrive_expect_tx(&base_full[0], bytes);
-          tma_load_2d(const_cast<BT*>(stage), &base_map, &base_full[0], v0, 0);
+          mbar_arrive_expect_tx(&base_full[sb], bytes);
+          tma_load_2d(const_cast<BT*>(stage) + (size_t)sb * tile_floats, &base_map,
+                      &base_full[sb], v0, 0);
         } else {
           const int buf = t & 1;
           if (!mbar_wait(&tile_free[buf], ((uint32_t)(t >> 1) & 1u) ^ 1u, kSpin)) {
@@ -700,14 +710,15 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         const uint32_t ph = (uint32_t)(t >> 1) & 1u;
         const int v0 = (chunk + t * P.n_chunks) * kTileV;
         float* tile = tiles + (size_t)buf * tile_floats;
-        // bf16 logits arrive in the staging tile, so the f32 buffer is
+        // bf16 logits arrive in a staging tile, so the f32 buffer is
         // written here: it must be released (tile t-2 read by the compute
         // warps and the store) first; f32 logits were loaded into it by TMA
         // only after that release
+        const int sb = kStaged ? stage_of(t) : buf;
+        const BT* stage_t = stage + (size_t)sb * tile_floats;
         bool ok = !*abort_flag &&
                   (!kStaged || mbar_wait(&tile_free[buf], ph ^ 1u, kSpin)) &&
-                  mbar_wait(kStaged ? &base_full[0] : &base_full[buf],
-                            kStaged ? ((uint32_t)t & 1u) : ph, kSpin) &&
+                  mbar_wait(&base_full[sb], kStaged ? stage_parity(t) : ph, kSpin) &&
                   mbar_wait(&acc_full[buf], ph, kSpin);
         ok = __all_sync(0xffffffffu, ok);  // tcgen05.ld needs the whole warp
         if (ok) {
@@ -728,7 +739,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
 #pragma unroll
               for (int j = 0; j < 16; ++j)
                 x[j] = kStaged ? __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(
-                                                     stage)[(c0 + j) * kTileV + m] << 16)
+                                                     stage_t)[(c0 + j) * kTileV + m] << 16)
                                : col[(c0 + j) * kTileV];
               tmem_ld_wait();
 #pragma unroll
@@ -744,7 +755,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
                 float x;
                 if (kStaged)
                   x = __uint_as_float(
-                      (uint32_t)reinterpret_cast<const uint16_t*>(stage)[c * kTileV + m] << 16);
+                      (uint32_t)reinterpret_cast<const uint16_t*>(stage_t)[c * kTileV + m] << 16);
                 else
                   x = col[c * kTileV];
                 col[c * kTileV] = ((pw >> j) & 1u) ? bias[j] : __fadd_rn(x, bias[j]);
@@ -762,7 +773,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
           fail(kDevErrTimeout);
         }
         mbar_arrive(&acc_empty[buf]);
-        if (kStaged) mbar_arrive(stage_free);
+        if (kStaged) mbar_arrive(&stage_free[sb]);
         fence_proxy_async_smem();         // the tile store reads these writes
         named_sync(1, kDrainThreads);     // the whole tile is drained
         if (storer && !*abort_flag) {
@@ -965,9 +976,9 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
         mbar_wait(&full[s], (uint32_t)(last / S) & 1u, kSpin >> 4);
       }
     } else if (lane == 1 && base_issued > 0) {
-      if (kStaged) {  // one staging buffer: its last load is the latest phase
+      if (kStaged && P.stage_bufs == 1) {  // its last load is the latest phase
         mbar_wait(&base_full[0], (uint32_t)(base_issued - 1) & 1u, kSpin >> 4);
-      } else {        // the last load of each of the two tile buffers
+      } else {  // the last load of each of the two tile or staging buffers
         for (int t = base_issued - 2 < 0 ? 0 : base_issued - 2; t < base_issued; ++t)
           mbar_wait(&base_full[t & 1], (uint32_t)(t >> 1) & 1u, kSpin >> 4);
       }
@@ -1001,25 +1012,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct Layout {
-  int bpad, stages;
+  int bpad, stages, stage_bufs;
   uint32_t u_off, tile_off, stage_off, rows_off, rstate_off, bar_off;
   size_t smem;
 };
 
-// Shared memory: the Wb ring, u, two float32 tile buffers [bpad][128], a
-// bf16 staging tile when the drafter logits are bf16, row info, barriers.
+// Shared memory: the Wb ring, u, two float32 tile buffers [bpad][128], one
+// or two bf16 staging tiles when the drafter logits are bf16, row info,
+// barriers.  Two staging tiles let the load of tile t+1's drafter logits
+// overlap the drain of tile t (a single one serialises them: measured
+// 336.9 -> 321.7 us per B=44 block); they are used while the Wb ring keeps
+// at least one tile of r = 256 (four stages), else one.
 Layout make_layout(int B, int r, int base_elt) {
   Layout L;
   L.bpad = (B + 15) / 16 * 16;
   const size_t u = (size_t)L.bpad * r * 2;
   const size_t tiles = 2 * (size_t)L.bpad * kTileV * 4;
-  const size_t stage = base_elt == 2 ? (size_t)L.bpad * kTileV * 2 : 0;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowConst), 16);
   const size_t rstate = (size_t)kComputeWarps * kMaxRows * 16;
-  const size_t bars = (2 * kMaxStages + 13) * 8 + 16;
-  const size_t fixed = u + tiles + stage + rows + rstate + bars + 1024;
-  L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
-  if (L.stages > kMaxStages) L.stages = kMaxStages;
+  const size_t bars = (2 * kMaxStages + 14) * 8 + 16;
+  size_t stage = 0;
+  for (int nsb = base_elt == 2 ? 2 : 0; nsb >= 0; --nsb) {
+    stage = (size_t)nsb * L.bpad * kTileV * 2;
+    L.stage_bufs = nsb;
+    const size_t fixed = u + tiles + stage + rows + rstate + bars + 1024;
+    L.stages = fixed < kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
+    if (L.stages > kMaxStages) L.stages = kMaxStages;
+    if (nsb <= 1 || L.stages >= 4) break;
+  }
   L.u_off = (uint32_t)((size_t)L.stages * kStageBytes);
   L.tile_off = (uint32_t)(L.u_off + u);
   L.stage_off = (uint32_t)(L.tile_off + tiles);
@@ -1120,6 +1140,7 @@ cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
   P.k = k;
   P.bpad = L.bpad;
   P.stages = L.stages;
+  P.stage_bufs = L.stage_bufs;
   P.stall_first_wait = stall_first_wait_requested() ? 1 : 0;
   P.tiles_total = (a.V + kTileV - 1) / kTileV;
   P.n_chunks = n_chunks;

@@ -472,18 +472,37 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl")
 
-    w = wl.make_config(CONFIG_ID)
+    w = wl.make_config(args.config if args.mode == "ncu" else CONFIG_ID)
     if args.positions != w.K:
         w.K = args.positions
         w.base = np.ascontiguousarray(w.base[:, :w.K])
     B, K, V, r = w.B, w.K, w.V, w.r
 
     if args.mode == "ncu":
+        # a small, self-ending workload for profiler captures: a few eager
+        # blocks, then (--ncu-extra) one call of each verification rule and
+        # of the target sampler on the block's outputs
         dev = wl.to_device(w, device)
         for _ in range(args.blocks):
-            pkg.draft_block(dev["base"], dev["U"], dev["Wb"], dev["d0"],
-                            dev["seed"], dev["offset"], w.T,
-                            greedy=dev["greedy"], pad_row=dev["pad_row"])
+            tokens, logits, probs = pkg.draft_block(
+                dev["base"], dev["U"], dev["Wb"], dev["d0"], dev["seed"],
+                dev["offset"], w.T, greedy=dev["greedy"], pad_row=dev["pad_row"])
+        if args.ncu_extra:
+            gen = torch.Generator(device=device)
+            gen.manual_seed(5)
+            tl = torch.cat([logits, logits[:, -1:]], dim=1)
+            tl = tl + torch.randn(tl.shape, device=device, generator=gen)
+            target = torch.softmax(tl.nan_to_num(neginf=-1e30), dim=-1)
+            pkg.verify_standard(probs, target, tokens, dev["seed"], dev["offset"])
+            pkg.verify_block(probs, target, tokens, dev["seed"], dev["offset"])
+            del target
+            rows = tl.reshape(B * (K + 1), V).contiguous()
+            del tl
+            pkg.sample_temperature(
+                rows, dev["seed"].repeat_interleave(K + 1),
+                dev["offset"].repeat_interleave(K + 1), T=1.0,
+                position=torch.arange(K + 1, dtype=torch.int32,
+                                      device=device).repeat(B))
         torch.cuda.synchronize()
         return 0
 
@@ -729,6 +748,12 @@ def main():
                          "fewer shrink the device footprint for captures)")
     ap.add_argument("--blocks", type=int, default=2,
                     help="eager blocks run by --mode ncu")
+    ap.add_argument("--config", type=int, default=CONFIG_ID,
+                    choices=[1, 2, 3, 4, 5],
+                    help="workload of --mode ncu (4 = the benchmark block)")
+    ap.add_argument("--ncu-extra", action="store_true",
+                    help="--mode ncu: also one call of each verification "
+                         "rule and of the target sampler")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
