@@ -106,13 +106,12 @@ __device__ __forceinline__ float test_scale(const Best& st) {
              : 0x1p32f * kSlack * expf(-st.score);
 }
 
-// One Philox block of the sweep: weights, candidate test, exact scores of
-// the candidates, warp merge.  Warp-uniform control flow.  c is
-// test_scale(st), kept up to date here.
+// One Philox block of the sweep, with its noise words w: weights, candidate
+// test, exact scores of the candidates, warp merge.  Warp-uniform control
+// flow.  c is test_scale(st), kept up to date here.
 __device__ __forceinline__ void sweep_block(Best& st, float& c, bool& any, int j,
                                             float4 pv, float4 qv, bool resid,
-                                            float wscale, const uint4& pre,
-                                            const uint4 (&rk)[4]) {
+                                            float wscale, const uint4 w) {
   float wt[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
@@ -121,7 +120,6 @@ __device__ __forceinline__ void sweep_block(Best& st, float& c, bool& any, int j
     wt[e] = d > 0.0f ? d : 0.0f;  // NaN and non-positive weights: 0
     any |= wt[e] > 0.0f;
   }
-  const uint4 w = philox_folded(pre, rk, (uint32_t)j);
   float thr[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) thr[e] = wt[e] > 0.0f ? __fmul_ru(wt[e], c) : 0.0f;
@@ -173,9 +171,13 @@ __device__ Slot draw_row(cg::cluster_group& cluster, const float* __restrict__ p
     float4 p0, q0, p1, q1;
     load_block<kVec>(p, q, V, j0, hi, p0, q0);
     load_block<kVec>(p, q, V, j1, hi, p1, q1);
-    sweep_block(st, c, any, j0, p0, q0, resid, wscale, pre, rk);
+    // the two blocks' noise first: two independent Philox chains the
+    // scheduler interleaves (43.1 -> 41.5 us for the B=88 block)
+    const uint4 w0 = philox_folded(pre, rk, (uint32_t)j0);
+    const uint4 w1 = philox_folded(pre, rk, (uint32_t)j1);
+    sweep_block(st, c, any, j0, p0, q0, resid, wscale, w0);
     if (base + kStride < hi)
-      sweep_block(st, c, any, j1, p1, q1, resid, wscale, pre, rk);
+      sweep_block(st, c, any, j1, p1, q1, resid, wscale, w1);
   }
   any = __any_sync(0xffffffffu, any);
   if (lane == 0) {
