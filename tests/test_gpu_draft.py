@@ -96,6 +96,11 @@ SMALL_CASES = [
     (128, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),        # largest batch
     (97, 1, 8192, 192, wl.F32, wl.BF16, 1.3, {}),
     (1, 3, 200064, 256, wl.BF16, wl.BF16, 1.0, {"n_spikes": 32}),
+    # bf16 drafter logits: with r = 256, B > 64 gets one staging tile (two
+    # would leave the Wb ring fewer than four stages), B <= 64 two
+    (88, 2, 4096, 256, wl.BF16, wl.BF16, 1.0, {"greedy_rows": [5], "pad_rows": [87]}),
+    (96, 3, 2056, 128, wl.BF16, wl.BF16, 0.8, {}),
+    (48, 2, 3072, 256, wl.BF16, wl.BF16, 1.0, {"n_spikes": 4}),
 ]
 
 

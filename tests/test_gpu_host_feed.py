@@ -60,6 +60,9 @@ CASES = [
     # tensor-core path with bf16 logits and T != 1
     dict(B=16, K=4, V=40000, r=128, seed=82, base_dtype=wl.BF16,
          w_dtype=wl.BF16, T=0.7),
+    # bf16 logits at B = 72, r = 256 (one staging tile)
+    dict(B=72, K=2, V=6144, r=256, seed=85, base_dtype=wl.BF16,
+         w_dtype=wl.BF16),
     # FFMA path: f32 head, ragged vocabulary
     dict(B=5, K=2, V=3001, r=32, seed=83, base_dtype=wl.F32, w_dtype=wl.F32),
 ]

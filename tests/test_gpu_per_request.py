@@ -45,9 +45,12 @@ CASES = [
     # tensor-core kernel: bf16 head, greedy and padding requests
     dict(B=24, K=3, V=20000, r=256, seed=61, base_dtype=wl.F32,
          w_dtype=wl.BF16, greedy_rows=[3], pad_rows=[23], n_spikes=4),
-    # tensor-core kernel with bf16 drafter logits
+    # tensor-core kernel with bf16 drafter logits (two staging tiles)
     dict(B=10, K=4, V=40000, r=128, seed=62, base_dtype=wl.BF16,
          w_dtype=wl.BF16),
+    # bf16 drafter logits at B = 88, r = 256 (one staging tile)
+    dict(B=88, K=2, V=8192, r=256, seed=66, base_dtype=wl.BF16,
+         w_dtype=wl.BF16, greedy_rows=[2], pad_rows=[87]),
     # FFMA kernel: f32 head, ragged vocabulary
     dict(B=6, K=2, V=3001, r=32, seed=63, base_dtype=wl.F32, w_dtype=wl.F32),
 ]
