@@ -139,7 +139,11 @@ DSPARK_API dspark_status dspark_draft_block(
  * `stream` and returns, per kernel class, the summed event time and the
  * number of launches:
  *   stage_ms[3], stage_launches[3]  (host arrays) -- [0] the K position
- *   kernels, [1] the K pick kernels, [2] the proposal writer.
+ *   kernels, [1] the pick kernels (one after the last position on the
+ *   tensor-core path, one after every position on the FFMA path), [2] the
+ *   proposal writer.  The events between launches remove the overlap of
+ *   consecutive positions (programmatic dependent launch); see
+ *   dspark_draft_block_timeline for times in the block's own schedule.
  * Outputs are identical to dspark_draft_block's.  Because it synchronises
  * and creates events, it must not be captured in a CUDA graph.
  */
