@@ -645,9 +645,16 @@ def run_ours(args, rank, world):
     sampler = {"us_per_call": g0.elapsed_time(g1) / 10 * 1e3,
                "rows": B * (K + 1), "V": V,
                "bytes": 3 * B * (K + 1) * V * 4,
+               "compulsory_bytes": 2 * B * (K + 1) * V * 4,
                "note": "temperature-only sampling of the block's target rows "
-                       "(token and probabilities per row)"}
+                       "(token and probabilities per row); bytes: the three "
+                       "launches' traffic (the logits read by the statistics "
+                       "and again by the probability writer, the "
+                       "probabilities written), compulsory_bytes: the logits "
+                       "read once and the probabilities written once"}
     sampler["hbm_frac"] = sampler["bytes"] / (sampler["us_per_call"] * 1e-6) / 1e9 / peak
+    sampler["hbm_frac_compulsory"] = (sampler["compulsory_bytes"] /
+                                      (sampler["us_per_call"] * 1e-6) / 1e9 / peak)
     del tl_rows, smp_probs
     acc_len = torch.empty(B, dtype=torch.int32, device=device)
     emitted = torch.empty(B, dtype=torch.int32, device=device)

@@ -88,13 +88,18 @@ SMALL_CASES = [
     (2, 3, 1536, 64, wl.F32, wl.F32, 0.05, {}),           # extreme T
     (2, 3, 1536, 64, wl.F32, wl.F32, 20.0, {}),
     (1, 1, 1, 16, wl.F32, wl.F32, 1.0, {}),               # V = 1
+    (2, 20, 777, 32, wl.BF16, wl.F32, 0.9, {}),           # a long chain
+    (128, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),        # bf16 head, B above
+    (300, 2, 512, 64, wl.F32, wl.BF16, 1.0, {"pad_rows": [299]}),  # the tc limit
+    (1024, 1, 64, 16, wl.F32, wl.F32, 1.0, {}),           # the largest batch
     (3, 2, 130, 256, wl.BF16, wl.BF16, 1.0, {}),          # r = 256, V < 2 tiles
     # shapes the tensor-core kernel takes (bf16 head, r % 64 == 0, V % 8 == 0)
     (16, 3, 4096, 64, wl.F32, wl.BF16, 1.0, {}),
     (5, 2, 1000, 128, wl.BF16, wl.BF16, 0.7, {"greedy_rows": [1]}),  # ragged tile
     (33, 2, 2056, 256, wl.F32, wl.BF16, 1.0, {"pad_rows": [0, 32]}),
-    (128, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),        # largest batch
-    (97, 1, 8192, 192, wl.F32, wl.BF16, 1.3, {}),
+    (96, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),         # its largest batch
+    (95, 1, 8192, 192, wl.F32, wl.BF16, 1.3, {}),
+    (3, 64, 520, 64, wl.F32, wl.BF16, 1.0, {"greedy_rows": [1]}),  # K = 64
     (1, 3, 200064, 256, wl.BF16, wl.BF16, 1.0, {"n_spikes": 32}),
     # bf16 drafter logits: with r = 256, B > 64 gets one staging tile (two
     # would leave the Wb ring fewer than four stages), B <= 64 two
@@ -105,8 +110,10 @@ SMALL_CASES = [
 
 
 def tc_eligible(case):
+    """Shapes the tensor-core kernel takes (bf16 head, r a multiple of 64 up
+    to 256, V % 8 == 0, at most 96 requests)."""
     B, K, V, r, bdt, wdt = case[:6]
-    return wdt == wl.BF16 and r % 64 == 0 and V % 8 == 0 and B <= 128
+    return wdt == wl.BF16 and r % 64 == 0 and V % 8 == 0 and B <= 96
 
 
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")
@@ -141,6 +148,23 @@ def test_ffma_kernel_parity_on_tensor_core_shapes(case, monkeypatch):
     st = check_block_against_oracle(w, tokens, logits, probs,
                                     rows=default_rows(B, K, max_rows=64))
     assert st["near_tie_token_diffs"] <= 1
+
+
+@pytest.mark.parametrize("case", [c for c in SMALL_CASES if tc_eligible(c)],
+                         ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")
+def test_tensor_core_kernel_takes_the_eligible_shapes(case, monkeypatch):
+    """The shapes the parity tests count as tensor-core shapes do run the
+    tensor-core kernel: forcing it succeeds and gives the default call's
+    outputs bit for bit."""
+    B, K, V, r, bdt, wdt, T, extra = case
+    w = wl.make_custom(B, K, V, r, seed=300 + V + B, base_dtype=bdt,
+                       w_dtype=wdt, T=T, w_std=0.2, **extra)
+    dev = to_device(w)
+    default = _np(run_draft(w, dev))
+    monkeypatch.setenv("DSPARK_POSITION_KERNEL", "tc")
+    forced = _np(run_draft(w, dev))
+    for a, b in zip(default, forced):
+        np.testing.assert_array_equal(a, b)
 
 
 def test_forcing_tensor_core_kernel_on_unsupported_shape_fails(monkeypatch):
