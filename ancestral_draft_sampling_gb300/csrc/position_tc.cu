@@ -84,7 +84,10 @@ constexpr uint32_t kTmemCols = 256;                // two accumulators
 constexpr uint32_t kAccCols = 128;
 constexpr uint32_t kSpin = 1u << 22;
 constexpr uint32_t kStallPolls = 1u << 12;  // the stalled wait's poll limit
-constexpr int kMinStages = 3;
+// Fewest Wb stages the kernel runs with.  Two is what bf16 drafter logits
+// leave at r = 256 and 81..96 requests (one staging tile): 519 us for a
+// B=88, K=7, V=200064 block, against 4255 us on the FFMA kernel.
+constexpr int kMinStages = 2;
 constexpr int kMaxStages = 8;
 constexpr size_t kSmemLimit = 232448;              // 227 KB per CTA
 constexpr float kLog2e = 1.4426950408889634f;

@@ -131,3 +131,21 @@ def test_config5_drafts_verified_against_its_target():
     # block verification accepts at least as much as the standard rule in
     # expectation; over 64 requests allow a small shortfall
     assert means["block"] >= means["standard"] - 0.25
+
+
+def test_bf16_logits_at_96_requests_every_row():
+    """bf16 drafter logits with 96 requests at r = 256: one staging tile and
+    a two-stage Wb ring in the tensor-core kernel.  Every row of a K=3 block
+    over the full vocabulary against the oracle, and every stored proposal
+    against the softmax of its own float32 logits."""
+    w = wl.make_custom(96, 3, 200064, 256, seed=1096, base_std=4.0,
+                       base_dtype=wl.BF16, w_dtype=wl.BF16, n_spikes=32,
+                       greedy_rows=[7], pad_rows=[95])
+    dev = to_device(w)
+    tokens, logits, probs = (t.cpu().numpy() for t in run_draft(w, dev))
+    del dev
+    _properties(w, tokens, logits, probs)
+    assert check_probs_against_own_logits(w, tokens, logits, probs) == w.B * w.K
+    st = check_block_against_oracle(w, tokens, logits, probs)
+    assert st["rows"] + st["rows_after_divergence"] == w.B * w.K
+    assert st["near_tie_token_diffs"] <= 1
