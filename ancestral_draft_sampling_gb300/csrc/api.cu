@@ -8,11 +8,13 @@
 // (token d_k, row max and sum-exp) after the last tensor-core position or
 // after every FFMA position, and one proposal writer for all positions.  No
 // host synchronisation, so the whole call can be captured in a CUDA graph.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "dspark_common.cuh"
 
@@ -111,9 +113,9 @@ dspark_status prepare_draft(
 // Event pairs around each kernel class: [0] position kernels, [1] picks,
 // [2] proposal writer.  Accumulated milliseconds are returned.
 struct StageTimer {
-  cudaEvent_t ev[2 * (DSPARK_MAX_K * 2 + 1)];
+  std::vector<cudaEvent_t> ev;  // two per launch
+  std::vector<int> cls;         // one per launch
   int n = 0;
-  int cls[DSPARK_MAX_K * 2 + 1];
 };
 
 dspark_status timed_launch(StageTimer* t, int cls, cudaStream_t stream,
@@ -121,6 +123,7 @@ dspark_status timed_launch(StageTimer* t, int cls, cudaStream_t stream,
                                              cudaStream_t),
                            const DraftArgs& a, int k, int n) {
   if (t) {
+    if (t->n >= (int)t->cls.size()) return DSPARK_ERR_INVALID_ARG;
     if (cudaEventRecord(t->ev[2 * t->n], stream) != cudaSuccess)
       return DSPARK_ERR_CUDA;
   }
@@ -173,9 +176,44 @@ struct HostFeed {
   cudaEvent_t* ready;     // K + 1 events
 };
 
+// Requests b0 .. b0 + n - 1 of a block as a block of their own: the same
+// heads, workspace statistics and error word; their rows of every other
+// array (per-request slots index the full proposal array).
+DraftArgs request_group(const DraftArgs& a, int b0, int n) {
+  DraftArgs g = a;
+  const size_t rows = (size_t)b0 * a.K;
+  const size_t elt = a.base_dtype == DSPARK_F32 ? 4 : 2;
+  g.B = n;
+  g.base = static_cast<const char*>(a.base) + rows * a.V * elt;
+  g.d0 = a.d0 + b0;
+  g.seed = a.seed + b0;
+  g.offset = a.offset + b0;
+  if (a.greedy) g.greedy = a.greedy + b0;
+  if (a.pad_row) g.pad_row = a.pad_row + b0;
+  if (a.temperature) g.temperature = a.temperature + b0;
+  g.tokens = a.tokens + rows;
+  g.logits = a.logits + rows * a.V;
+  if (a.slot) g.slot = a.slot + b0;
+  else if (a.probs) g.probs = a.probs + rows * a.V;
+  g.rowstats = a.rowstats + rows * 2;
+  g.hints = a.hints + (size_t)b0 * kHintRowKeys;
+  return g;
+}
+
+// Launches one draft block makes (an upper bound when the kernel is not
+// yet known): per request group, K positions and K picks at most, then the
+// proposal writer.
+int block_launch_bound(int B, int K) {
+  return position_tc_groups(B) * 2 * K + 1;
+}
+
 // The launch sequence of one draft block.  chain_end (measurement only):
 // an event recorded as an external event node between the position chain
 // (the memset, the positions and their picks) and the proposal writer.
+// A block of more requests than the tensor-core kernel takes in one launch
+// runs as consecutive request groups (position_tc_groups), each its own
+// chain of positions over the same heads; the proposal writer then covers
+// all rows at once.
 dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
                         StageTimer* t, const HostFeed* feed = nullptr,
                         cudaEvent_t chain_end = nullptr) {
@@ -213,30 +251,37 @@ dspark_status run_block(const DraftArgs& a, cudaStream_t stream,
   // d_{k-1} from the decision keys and merges position k-1's statistics
   // itself; one pick after the last position finishes the block.  Each
   // FFMA position is followed by its pick.
-  for (int k = 0; k < a.K; ++k) {
-    if (feed && cudaStreamWaitEvent(stream, feed->ready[k], 0) != cudaSuccess)
-      return DSPARK_ERR_CUDA;
-    dspark_status st = timed_launch(
-        t, 0, stream, tc ? launch_position_tc : launch_position_generic, a, k,
-        want);
-    if (st != DSPARK_OK) return st;
-    if (!tc || k == a.K - 1) {
-      st = timed_launch(t, 1, stream, tc ? launch_pick_keys : launch_pick_plain,
-                        a, k, n_chunks);
-      if (st != DSPARK_OK) return st;
-    }
-    // with host-fed logits the GPU would idle until the next slice arrives:
-    // write each position's proposals as soon as its (M, S) exist (after
-    // its pick, or after the next tensor-core position has merged them)
-    if (feed) {
-      int lo = k, hi = k;  // FFMA: position k's pick has just run
-      if (tc) {            // position k merged k-1; the last pick ran for K-1
-        lo = k - 1 < 0 ? 0 : k - 1;
-        hi = k == a.K - 1 ? k : k - 1;
-      }
-      if (hi >= lo &&
-          from_cuda(launch_proposals(a, lo, hi - lo + 1, stream)) != DSPARK_OK)
+  const int n_groups = tc ? position_tc_groups(a.B) : 1;
+  const int per_group = (a.B + n_groups - 1) / n_groups;
+  for (int b0 = 0; b0 < a.B; b0 += per_group) {
+    const DraftArgs g = n_groups == 1 ? a
+                                      : request_group(a, b0, std::min(per_group, a.B - b0));
+    for (int k = 0; k < g.K; ++k) {
+      if (feed && cudaStreamWaitEvent(stream, feed->ready[k], 0) != cudaSuccess)
         return DSPARK_ERR_CUDA;
+      dspark_status st = timed_launch(
+          t, 0, stream, tc ? launch_position_tc : launch_position_generic, g, k,
+          want);
+      if (st != DSPARK_OK) return st;
+      if (!tc || k == g.K - 1) {
+        st = timed_launch(t, 1, stream, tc ? launch_pick_keys : launch_pick_plain,
+                          g, k, n_chunks);
+        if (st != DSPARK_OK) return st;
+      }
+      // with host-fed logits the GPU would idle until the next slice
+      // arrives: write each position's proposals as soon as its (M, S)
+      // exist (after its pick, or after the next tensor-core position has
+      // merged them)
+      if (feed) {
+        int lo = k, hi = k;  // FFMA: position k's pick has just run
+        if (tc) {            // position k merged k-1; the last pick ran for K-1
+          lo = k - 1 < 0 ? 0 : k - 1;
+          hi = k == g.K - 1 ? k : k - 1;
+        }
+        if (hi >= lo &&
+            from_cuda(launch_proposals(g, lo, hi - lo + 1, stream)) != DSPARK_OK)
+          return DSPARK_ERR_CUDA;
+      }
     }
   }
   if (feed) return DSPARK_OK;
@@ -460,7 +505,10 @@ dspark_status dspark_draft_block_profile(
       workspace_bytes, a);
   if (st != DSPARK_OK) return st;
   StageTimer t;
-  const int n_ev = 2 * (2 * K + 1);
+  const int n_launch = block_launch_bound(B, K);
+  const int n_ev = 2 * n_launch;
+  t.ev.assign(n_ev, nullptr);
+  t.cls.assign(n_launch, 0);
   int created = 0;
   for (; created < n_ev; ++created)
     if (cudaEventCreate(&t.ev[created]) != cudaSuccess) break;

@@ -404,6 +404,7 @@ __device__ __forceinline__ float request_temperature(const DraftArgs& a, int b) 
 cudaError_t launch_position_generic(const DraftArgs& a, int k, int n_chunks,
                                     cudaStream_t stream);
 bool position_tc_supported(const DraftArgs& a);
+int position_tc_groups(int B);
 int position_tc_chunks(int V, int sm_count);
 cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
                                cudaStream_t stream);

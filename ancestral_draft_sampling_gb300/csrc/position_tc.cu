@@ -1098,11 +1098,21 @@ cudaError_t launch_typed(const CUtensorMap& wb, const CUtensorMap& bm,
 
 }  // namespace
 
+// Request groups of a block on the tensor-core kernel: one launch per
+// position takes at most kMaxBpad requests, so a larger block runs as
+// ceil(B / kMaxBpad) groups of near-equal size (each reads Wb once per
+// position).
+int position_tc_groups(int B) {
+  return B <= kMaxBpad ? 1 : (B + kMaxBpad - 1) / kMaxBpad;
+}
+
 bool position_tc_supported(const DraftArgs& a) {
   const int elt = a.base_dtype == DSPARK_F32 ? 4 : 2;
+  const int n = position_tc_groups(a.B);
+  const int per_group = (a.B + n - 1) / n;
   return a.w_dtype == DSPARK_BF16 && a.r % kKChunk == 0 && a.r <= 256 &&
-         a.V % 8 == 0 && a.B <= kMaxBpad &&
-         make_layout(a.B, a.r, elt).stages >= kMinStages &&
+         a.V % 8 == 0 && per_group <= kMaxBpad &&
+         make_layout(per_group, a.r, elt).stages >= kMinStages &&
          encode_fn() != nullptr;
 }
 
@@ -1116,6 +1126,7 @@ int position_tc_chunks(int V, int sm_count) {
 cudaError_t launch_position_tc(const DraftArgs& a, int k, int n_chunks,
                                cudaStream_t stream) {
   if (!encode_fn()) return cudaErrorNotSupported;
+  if (a.B > kMaxBpad) return cudaErrorInvalidValue;  // a request group at most
   const int elt = a.base_dtype == DSPARK_F32 ? 4 : 2;
   const Layout L = make_layout(a.B, a.r, elt);
   CUtensorMap wb, bm, om;

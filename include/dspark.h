@@ -123,6 +123,12 @@ DSPARK_API size_t dspark_draft_workspace_bytes(int B, int K, int V, int r);
  *                aligned.
  * Alignment: every device pointer must be at least 16-byte aligned
  * (DSPARK_ERR_INVALID_ARG otherwise).
+ * Launches on `stream`, after one 2-D memset of the error word and the
+ * decision keys: with a bf16 head, r a multiple of 64 up to 256 and
+ * V % 8 == 0 the tensor-core kernel, K positions and one pick per request
+ * group (ceil(B / 96) groups of near-equal size, each a chain over the same
+ * heads), then one proposal writer; otherwise the FFMA kernel, K positions
+ * and K picks, then the writer.  No host synchronisation; graph capturable.
  */
 DSPARK_API dspark_status dspark_draft_block(
     const void* base_logits, dspark_dtype base_dtype, const void* U,
@@ -138,10 +144,10 @@ DSPARK_API dspark_status dspark_draft_block(
  * events recorded on `stream` around every launch.  It then synchronises
  * `stream` and returns, per kernel class, the summed event time and the
  * number of launches:
- *   stage_ms[3], stage_launches[3]  (host arrays) -- [0] the K position
- *   kernels, [1] the pick kernels (one after the last position on the
- *   tensor-core path, one after every position on the FFMA path), [2] the
- *   proposal writer.  The events between launches remove the overlap of
+ *   stage_ms[3], stage_launches[3]  (host arrays) -- [0] the position
+ *   kernels (K per request group), [1] the pick kernels (one after each
+ *   group's last position on the tensor-core path, one after every position
+ *   on the FFMA path), [2] the proposal writer.  The events between launches remove the overlap of
  *   consecutive positions (programmatic dependent launch); see
  *   dspark_draft_block_timeline for times in the block's own schedule.
  * Outputs are identical to dspark_draft_block's.  Because it synchronises

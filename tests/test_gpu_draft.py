@@ -89,8 +89,6 @@ SMALL_CASES = [
     (2, 3, 1536, 64, wl.F32, wl.F32, 20.0, {}),
     (1, 1, 1, 16, wl.F32, wl.F32, 1.0, {}),               # V = 1
     (2, 20, 777, 32, wl.BF16, wl.F32, 0.9, {}),           # a long chain
-    (128, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),        # bf16 head, B above
-    (300, 2, 512, 64, wl.F32, wl.BF16, 1.0, {"pad_rows": [299]}),  # the tc limit
     (1024, 1, 64, 16, wl.F32, wl.F32, 1.0, {}),           # the largest batch
     (3, 2, 130, 256, wl.BF16, wl.BF16, 1.0, {}),          # r = 256, V < 2 tiles
     # shapes the tensor-core kernel takes (bf16 head, r % 64 == 0, V % 8 == 0)
@@ -100,6 +98,10 @@ SMALL_CASES = [
     (96, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),         # its largest batch
     (95, 1, 8192, 192, wl.F32, wl.BF16, 1.3, {}),
     (3, 64, 520, 64, wl.F32, wl.BF16, 1.0, {"greedy_rows": [1]}),  # K = 64
+    # more than 96 requests: groups of at most 96, one chain each
+    (128, 2, 1024, 64, wl.BF16, wl.BF16, 1.0, {}),        # 2 groups of 64
+    (300, 2, 512, 64, wl.F32, wl.BF16, 1.0, {"pad_rows": [299], "greedy_rows": [97]}),
+    (1024, 2, 256, 64, wl.BF16, wl.BF16, 0.9, {}),        # 11 groups
     (1, 3, 200064, 256, wl.BF16, wl.BF16, 1.0, {"n_spikes": 32}),
     # bf16 drafter logits: with r = 256, B > 64 gets one staging tile (two
     # would leave the Wb ring fewer than four stages), B <= 64 two
@@ -111,9 +113,9 @@ SMALL_CASES = [
 
 def tc_eligible(case):
     """Shapes the tensor-core kernel takes (bf16 head, r a multiple of 64 up
-    to 256, V % 8 == 0, at most 96 requests)."""
+    to 256, V % 8 == 0; more than 96 requests run as request groups)."""
     B, K, V, r, bdt, wdt = case[:6]
-    return wdt == wl.BF16 and r % 64 == 0 and V % 8 == 0 and B <= 96
+    return wdt == wl.BF16 and r % 64 == 0 and r <= 256 and V % 8 == 0
 
 
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")

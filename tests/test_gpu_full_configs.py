@@ -149,3 +149,20 @@ def test_bf16_logits_at_96_requests_every_row():
     st = check_block_against_oracle(w, tokens, logits, probs)
     assert st["rows"] + st["rows_after_divergence"] == w.B * w.K
     assert st["near_tie_token_diffs"] <= 1
+
+
+def test_request_groups_every_row():
+    """200 requests over the full vocabulary run as three request groups of
+    at most 67 on the tensor-core kernel; every row against the oracle and
+    every stored proposal against the softmax of its own logits."""
+    w = wl.make_custom(200, 2, 200064, 256, seed=1200, base_std=4.0,
+                       base_dtype=wl.F32, w_dtype=wl.BF16, n_spikes=32,
+                       greedy_rows=[66, 67], pad_rows=[133, 199])
+    dev = to_device(w)
+    tokens, logits, probs = (t.cpu().numpy() for t in run_draft(w, dev))
+    del dev
+    _properties(w, tokens, logits, probs)
+    assert check_probs_against_own_logits(w, tokens, logits, probs) == w.B * w.K
+    st = check_block_against_oracle(w, tokens, logits, probs)
+    assert st["rows"] + st["rows_after_divergence"] == w.B * w.K
+    assert st["near_tie_token_diffs"] <= 1

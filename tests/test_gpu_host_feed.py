@@ -65,6 +65,9 @@ CASES = [
          w_dtype=wl.BF16),
     # FFMA path: f32 head, ragged vocabulary
     dict(B=5, K=2, V=3001, r=32, seed=83, base_dtype=wl.F32, w_dtype=wl.F32),
+    # 130 requests: two request groups, each position's proposals per group
+    dict(B=130, K=3, V=4096, r=64, seed=86, base_dtype=wl.F32,
+         w_dtype=wl.BF16, greedy_rows=[70]),
 ]
 
 

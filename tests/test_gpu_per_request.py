@@ -53,6 +53,9 @@ CASES = [
          w_dtype=wl.BF16, greedy_rows=[2], pad_rows=[87]),
     # FFMA kernel: f32 head, ragged vocabulary
     dict(B=6, K=2, V=3001, r=32, seed=63, base_dtype=wl.F32, w_dtype=wl.F32),
+    # 150 requests: two request groups of 75
+    dict(B=150, K=2, V=8192, r=128, seed=69, base_dtype=wl.F32,
+         w_dtype=wl.BF16, greedy_rows=[100], pad_rows=[149]),
 ]
 
 
@@ -81,14 +84,15 @@ def test_equal_temperatures_are_the_scalar_call(T):
         np.testing.assert_array_equal(a, b)
 
 
-def test_slots_receive_their_request_and_nothing_else():
-    w = wl.make_custom(10, 3, 9000, 64, seed=65, base_dtype=wl.F32,
+@pytest.mark.parametrize("B", [10, 130])  # 130: two request groups
+def test_slots_receive_their_request_and_nothing_else(B):
+    w = wl.make_custom(B, 3, 9000, 64, seed=65, base_dtype=wl.F32,
                        w_dtype=wl.BF16, w_std=0.2)
     dev = to_device(w)
     temps = _temps(w.B)
     _, _, plain = _per_request(w, dev, temps)
     rng = np.random.default_rng(66)
-    n_slots = 16
+    n_slots = B + 6
     slot = rng.permutation(n_slots)[:w.B]
     buf = torch.full((n_slots, w.K, w.V), -1.0, device="cuda")
     _, _, got = _per_request(w, dev, temps, slot=slot, draft_probs=buf)
