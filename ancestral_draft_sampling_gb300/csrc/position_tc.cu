@@ -463,7 +463,10 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
   // tiles chunk, chunk + n_chunks, ...: at any moment the CTAs work on
   // neighbouring tiles (measured faster than contiguous ranges)
   const int n_tiles = (P.tiles_total - 1 - chunk) / P.n_chunks + 1;
-  const int kchunks = a.r / kKChunk;
+  // r-chunks of kKChunk; the last one may be partial (r % 16 == 0): its Wb
+  // rows past r load as zeros (TMA fill) and the gather writes zeros into
+  // its u rows past r, so the MMA's K steps there add exactly 0
+  const int kchunks = (a.r + kKChunk - 1) / kKChunk;
   const int tile_floats = P.bpad * kTileV;
   // bf16 drafter logits: staging tile and phase of tile t (one or two
   // staging tiles, see make_layout)
@@ -651,7 +654,8 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
     grid_dependency_wait();
     {
     const int ct = threadIdx.x - 64;
-    const int pieces = a.r / 8;
+    const int pieces = kchunks * (kKChunk / 8);  // 16-byte pieces, whole chunks
+    const int valid = a.r / 8;                   // pieces that hold U values
     const int total = P.bpad * pieces;
     const uint16_t* U = static_cast<const uint16_t*>(a.U);
     for (int i0 = ct; i0 < total; i0 += kWorkThreads * kGatherBatch) {
@@ -669,7 +673,7 @@ position_tc_kernel(const __grid_constant__ CUtensorMap wb_map,
       for (int j = 0; j < kGatherBatch; ++j) {
         const int i = i0 + j * kWorkThreads, b = i / pieces, piece = i - b * pieces;
         val[j] = make_uint4(0u, 0u, 0u, 0u);
-        if (i < total && b < a.B) {
+        if (i < total && b < a.B && piece < valid) {
           int pv = prev[j];
           if ((unsigned)pv >= (unsigned)a.V) {
             if (piece == 0) a.control[0] = kDevErrBadToken;
@@ -1029,7 +1033,8 @@ struct Layout {
 Layout make_layout(int B, int r, int base_elt) {
   Layout L;
   L.bpad = (B + 15) / 16 * 16;
-  const size_t u = (size_t)L.bpad * r * 2;
+  // u: whole r-chunks of 64 (128-byte swizzled rows)
+  const size_t u = (size_t)L.bpad * ((r + kKChunk - 1) / kKChunk * kKChunk) * 2;
   const size_t tiles = 2 * (size_t)L.bpad * kTileV * 4;
   const size_t rows = align_up((size_t)L.bpad * sizeof(RowConst), 16);
   const size_t rstate = (size_t)kComputeWarps * kMaxRows * 16;
@@ -1110,7 +1115,7 @@ bool position_tc_supported(const DraftArgs& a) {
   const int elt = a.base_dtype == DSPARK_F32 ? 4 : 2;
   const int n = position_tc_groups(a.B);
   const int per_group = (a.B + n - 1) / n;
-  return a.w_dtype == DSPARK_BF16 && a.r % kKChunk == 0 && a.r <= 256 &&
+  return a.w_dtype == DSPARK_BF16 && a.r % 16 == 0 && a.r <= 256 &&
          a.V % 8 == 0 && per_group <= kMaxBpad &&
          make_layout(per_group, a.r, elt).stages >= kMinStages &&
          encode_fn() != nullptr;

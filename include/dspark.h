@@ -124,7 +124,7 @@ DSPARK_API size_t dspark_draft_workspace_bytes(int B, int K, int V, int r);
  * Alignment: every device pointer must be at least 16-byte aligned
  * (DSPARK_ERR_INVALID_ARG otherwise).
  * Launches on `stream`, after one 2-D memset of the error word and the
- * decision keys: with a bf16 head, r a multiple of 64 up to 256 and
+ * decision keys: with a bf16 head, r a multiple of 16 up to 256 and
  * V % 8 == 0 the tensor-core kernel, K positions and one pick per request
  * group (ceil(B / 96) groups of near-equal size, each a chain over the same
  * heads), then one proposal writer; otherwise the FFMA kernel, K positions

@@ -38,7 +38,7 @@ def _call(w, dev, ws):
     return _np(out)
 
 
-# the tensor-core kernel (bf16 head, r % 64 == 0, V % 8 == 0) and the FFMA one
+# the tensor-core kernel (bf16 head, r % 16 == 0, V % 8 == 0) and the FFMA one
 CASES = {
     "tensor_core": dict(B=6, K=3, V=4096, r=64, w_dtype=wl.BF16, kernel="tc"),
     "ffma": dict(B=5, K=3, V=3001, r=32, w_dtype=wl.F32, kernel="generic"),

@@ -84,14 +84,19 @@ SMALL_CASES = [
     (2, 2, 4099, 16, wl.F32, wl.BF16, 1.3, {}),           # odd V: scalar path
     (5, 3, 1000, 48, wl.BF16, wl.F32, 1.0, {"greedy_rows": [1, 3]}),
     (4, 3, 3000, 64, wl.F32, wl.BF16, 1.0, {"pad_rows": [0, 3]}),
-    (70, 2, 2048, 32, wl.BF16, wl.BF16, 1.0, {"n_spikes": 4}),  # two groups
+    (70, 2, 2048, 32, wl.BF16, wl.F32, 1.0, {"n_spikes": 4}),   # two CTA groups
     (2, 3, 1536, 64, wl.F32, wl.F32, 0.05, {}),           # extreme T
     (2, 3, 1536, 64, wl.F32, wl.F32, 20.0, {}),
     (1, 1, 1, 16, wl.F32, wl.F32, 1.0, {}),               # V = 1
     (2, 20, 777, 32, wl.BF16, wl.F32, 0.9, {}),           # a long chain
     (1024, 1, 64, 16, wl.F32, wl.F32, 1.0, {}),           # the largest batch
     (3, 2, 130, 256, wl.BF16, wl.BF16, 1.0, {}),          # r = 256, V < 2 tiles
-    # shapes the tensor-core kernel takes (bf16 head, r % 64 == 0, V % 8 == 0)
+    # shapes the tensor-core kernel takes (bf16 head, r % 16 == 0, V % 8 == 0)
+    (4, 2, 1024, 16, wl.F32, wl.BF16, 1.0, {}),           # r = 16: one K step
+    (9, 3, 2048, 32, wl.BF16, wl.BF16, 0.8, {"greedy_rows": [2]}),
+    (7, 2, 4096, 48, wl.F32, wl.BF16, 1.0, {"pad_rows": [6]}),
+    (20, 2, 3000, 80, wl.F32, wl.BF16, 1.3, {}),          # a whole and a part chunk
+    (12, 2, 2048, 208, wl.BF16, wl.BF16, 1.0, {"n_spikes": 4}),
     (16, 3, 4096, 64, wl.F32, wl.BF16, 1.0, {}),
     (5, 2, 1000, 128, wl.BF16, wl.BF16, 0.7, {"greedy_rows": [1]}),  # ragged tile
     (33, 2, 2056, 256, wl.F32, wl.BF16, 1.0, {"pad_rows": [0, 32]}),
@@ -112,10 +117,10 @@ SMALL_CASES = [
 
 
 def tc_eligible(case):
-    """Shapes the tensor-core kernel takes (bf16 head, r a multiple of 64 up
+    """Shapes the tensor-core kernel takes (bf16 head, r a multiple of 16 up
     to 256, V % 8 == 0; more than 96 requests run as request groups)."""
     B, K, V, r, bdt, wdt = case[:6]
-    return wdt == wl.BF16 and r % 64 == 0 and r <= 256 and V % 8 == 0
+    return wdt == wl.BF16 and r % 16 == 0 and r <= 256 and V % 8 == 0
 
 
 @pytest.mark.parametrize("case", SMALL_CASES, ids=lambda c: f"B{c[0]}K{c[1]}V{c[2]}r{c[3]}")

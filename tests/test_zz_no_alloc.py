@@ -40,7 +40,7 @@ def _compare(got, want):
 
 def test_noalloc_matches_workspace_entry_point_on_consecutive_calls():
     cases = [
-        # tensor-core path: bf16 head, r % 64 == 0, V % 8 == 0
+        # tensor-core path: bf16 head, r % 16 == 0, V % 8 == 0
         wl.make_custom(40, 3, 20000, 256, seed=71, base_dtype=wl.F32,
                        w_dtype=wl.BF16, w_std=0.2, greedy_rows=[3],
                        pad_rows=[39], n_spikes=4),
