@@ -11,8 +11,16 @@
 // CTA walks its chunk in 128-wide vocab tiles.  Warp w owns the requests
 // w, w+8, ... of the group; lane l owns the four consecutive vocab entries
 // 4l..4l+3 of the tile, which are exactly the four words of one Philox
-// block.
+// block.  The draw and the sum-exp are the warp draw of gumbel_draw.cuh
+// (a reference shared by the warp, a conservative candidate test, exact
+// scores for the admitted entries only), with each request's folded Philox
+// constants in shared memory.  Against an exact score for every entry (two
+// logarithms and a full Philox block each) it took B=88, K=7, V=200064
+// blocks with f32 heads from 1344 to 1058 us at r = 16, 1733 to 1427 us at
+// r = 64 and 4358 to 4092 us at r = 256 (where the FFMA contraction
+// dominates).
 #include "dspark_common.cuh"
+#include "gumbel_draw.cuh"
 
 namespace dspark {
 namespace {
@@ -83,10 +91,11 @@ __device__ __forceinline__ void store_logits4(float* row, int v, int V,
   }
 }
 
-// Scaled logit, the float32 IEEE quotient l / T (division by 1 is exact).
-__device__ __forceinline__ float scale(float l, float T) {
-  return T == 1.0f ? l : __fdiv_rn(l, T);
-}
+// A request's folded Philox constants (philox_fold).
+struct alignas(16) RowNoise {
+  uint4 pre;
+  uint4 rk[4];
+};
 
 template <typename WT, typename BT, bool kVec>
 __global__ void __launch_bounds__(kThreads)
@@ -95,6 +104,9 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
   const int r = a.r, V = a.V, B = a.B, K = a.K;
   float* u_s = reinterpret_cast<float*>(smem_raw);             // [kGroup][r]
   WT* w_s = reinterpret_cast<WT*>(u_s + (size_t)kGroup * r);   // [r][kTileV]
+  // [kGroup]: each request's folded Philox constants (noise stream 0 at
+  // position k)
+  RowNoise* noise_s = reinterpret_cast<RowNoise*>(w_s + (size_t)r * kTileV);
 
   const int chunk = blockIdx.x;
   const int g0 = blockIdx.y * kGroup;
@@ -119,10 +131,16 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
     }
     u_s[i] = x;
   }
+  for (int bl = threadIdx.x; bl < nb; bl += kThreads) {
+    const uint64_t sd = a.seed[g0 + bl], off = a.offset[g0 + bl];
+    philox_fold(noise_s[bl].pre, noise_s[bl].rk, (uint32_t)sd, (uint32_t)(sd >> 32),
+                (uint32_t)k | ((uint32_t)kNoiseDraft << 16), (uint32_t)off,
+                (uint32_t)(off >> 32));
+  }
 
-  ChunkStat st[kRowsPerWarp];
+  SampleState st[kRowsPerWarp];
 #pragma unroll
-  for (int i = 0; i < kRowsPerWarp; ++i) st[i] = empty_stat();
+  for (int i = 0; i < kRowsPerWarp; ++i) st[i] = sample_state_init();
 
   const int n_tiles = (V + kTileV - 1) / kTileV;
   const int t_begin = chunk * tiles_per_chunk;
@@ -188,26 +206,19 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
         const bool greedy = a.greedy != nullptr && a.greedy[b] != 0;
         float base4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
         if (!pad) load_base4<BT, kVec>(base + row * V, v, V, base4);
-        float l[4], s[4], score[4];
+        float l[4];
         const float T = request_temperature(a, b);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          l[e] = pad ? acc[q][e] : __fadd_rn(base4[e], acc[q][e]);
-          s[e] = scale(l[e], T);
-        }
+        for (int e = 0; e < 4; ++e) l[e] = pad ? acc[q][e] : __fadd_rn(base4[e], acc[q][e]);
         store_logits4<kVec>(a.logits + row * V, v, V, l);
-        if (greedy) {
+        // entries past V take no part in the draw or the sum
 #pragma unroll
-          for (int e = 0; e < 4; ++e) score[e] = s[e];
-        } else {
-          const uint4 w = noise_block(a.seed[b], a.offset[b], k, kNoiseDraft,
-                                      (uint32_t)v >> 2);
-          score[0] = __fadd_rn(s[0], gumbel_from_word(w.x));
-          score[1] = __fadd_rn(s[1], gumbel_from_word(w.y));
-          score[2] = __fadd_rn(s[2], gumbel_from_word(w.z));
-          score[3] = __fadd_rn(s[3], gumbel_from_word(w.w));
-        }
-        fold4(st[p + q], s, score, v, V);
+        for (int e = 0; e < 4; ++e)
+          if (v + e >= V) l[e] = -INFINITY;
+        const uint4 w = greedy ? make_uint4(0u, 0u, 0u, 0u)
+                               : philox_folded(noise_s[bl].pre, noise_s[bl].rk,
+                                               (uint32_t)v >> 2);
+        sample_block<false>(st[p + q], l, v >> 2, T, greedy, w);
       }
     }
   }
@@ -216,7 +227,12 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
   for (int i = 0; i < kRowsPerWarp; ++i) {
     const int bl = warp + kWarps * i;
     if (bl >= nb) break;
-    const ChunkStat red = warp_reduce_stat(st[i]);
+    ChunkStat cs;
+    cs.best = st[i].ref;
+    cs.idx = st[i].idx;
+    cs.m = st[i].m;
+    cs.s = st[i].sum;
+    const ChunkStat red = warp_reduce_stat(cs);
     if (lane == 0) *stat_slot(a.stats, 0, a.B, g0 + bl, chunk) = red;
   }
 }
@@ -225,7 +241,7 @@ template <typename WT, typename BT, bool kVec>
 cudaError_t launch_typed(const DraftArgs& a, int k, int n_chunks,
                          cudaStream_t stream) {
   const size_t smem = (size_t)kGroup * a.r * sizeof(float) +
-                      (size_t)a.r * kTileV * sizeof(WT);
+                      (size_t)a.r * kTileV * sizeof(WT) + kGroup * sizeof(RowNoise);
   auto kern = position_generic_kernel<WT, BT, kVec>;
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
