@@ -93,6 +93,7 @@ SMALL_CASES = [
     (3, 2, 130, 256, wl.BF16, wl.BF16, 1.0, {}),          # r = 256, V < 2 tiles
     # shapes the tensor-core kernel takes (bf16 head, r % 16 == 0, V % 8 == 0)
     (4, 2, 1024, 16, wl.F32, wl.BF16, 1.0, {}),           # r = 16: one K step
+    (3, 2, 8, 64, wl.F32, wl.BF16, 1.0, {"greedy_rows": [0]}),  # V = 8: one part tile
     (9, 3, 2048, 32, wl.BF16, wl.BF16, 0.8, {"greedy_rows": [2]}),
     (7, 2, 4096, 48, wl.F32, wl.BF16, 1.0, {"pad_rows": [6]}),
     (20, 2, 3000, 80, wl.F32, wl.BF16, 1.3, {}),          # a whole and a part chunk
