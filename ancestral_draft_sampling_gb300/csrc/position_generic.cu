@@ -97,8 +97,15 @@ struct alignas(16) RowNoise {
   uint4 rk[4];
 };
 
-template <typename WT, typename BT, bool kVec>
-__global__ void __launch_bounds__(kThreads)
+// kMinBlocks: 2 where the shared memory lets two CTAs share an SM (the
+// registers are then held to 128), else 1.  With the drafter logits of a
+// pass loaded before its contraction, B=88, K=7, V=200064 blocks with f32
+// heads took 1058 -> 898 us at r = 16, 1429 -> 1303 us at r = 64 and
+// 4102 -> 3827 us at r = 256 (one CTA per SM by shared memory; 4171 us
+// with the two-CTA bound there).  The small first configuration (f32 head)
+// went from 33.5 to 36.8 us.
+template <typename WT, typename BT, bool kVec, int kMinBlocks>
+__global__ void __launch_bounds__(kThreads, kMinBlocks)
 position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int r = a.r, V = a.V, B = a.B, K = a.K;
@@ -170,6 +177,18 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
 #pragma unroll
     for (int p = 0; p < kRowsPerWarp; p += kRowsPerPass) {
       if (warp + kWarps * p >= nb) break;
+      // the pass's drafter logits first: their loads are in flight during
+      // the contraction below
+      float base4[kRowsPerPass][4];
+#pragma unroll
+      for (int q = 0; q < kRowsPerPass; ++q) {
+        const int bl = warp + kWarps * (p + q);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) base4[q][e] = 0.0f;
+        if (bl < nb && !(a.pad_row != nullptr && a.pad_row[g0 + bl] != 0))
+          load_base4<BT, kVec>(base + ((size_t)(g0 + bl) * K + k) * V, v0 + 4 * lane, V,
+                               base4[q]);
+      }
       float acc[kRowsPerPass][4];
 #pragma unroll
       for (int q = 0; q < kRowsPerPass; ++q)
@@ -204,12 +223,10 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
         const size_t row = (size_t)b * K + k;
         const bool pad = a.pad_row != nullptr && a.pad_row[b] != 0;
         const bool greedy = a.greedy != nullptr && a.greedy[b] != 0;
-        float base4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        if (!pad) load_base4<BT, kVec>(base + row * V, v, V, base4);
         float l[4];
         const float T = request_temperature(a, b);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) l[e] = pad ? acc[q][e] : __fadd_rn(base4[e], acc[q][e]);
+        for (int e = 0; e < 4; ++e) l[e] = pad ? acc[q][e] : __fadd_rn(base4[q][e], acc[q][e]);
         store_logits4<kVec>(a.logits + row * V, v, V, l);
         // entries past V take no part in the draw or the sum
 #pragma unroll
@@ -242,7 +259,10 @@ cudaError_t launch_typed(const DraftArgs& a, int k, int n_chunks,
                          cudaStream_t stream) {
   const size_t smem = (size_t)kGroup * a.r * sizeof(float) +
                       (size_t)a.r * kTileV * sizeof(WT) + kGroup * sizeof(RowNoise);
-  auto kern = position_generic_kernel<WT, BT, kVec>;
+  // two CTAs per SM if their shared memory (and the 1 KB each reserves) fits
+  const bool two = 2 * (smem + 1024) <= 228 * 1024;
+  auto kern = two ? position_generic_kernel<WT, BT, kVec, 2>
+                  : position_generic_kernel<WT, BT, kVec, 1>;
   cudaError_t err = cudaFuncSetAttribute(
       kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
