@@ -91,10 +91,15 @@ __device__ __forceinline__ void store_logits4(float* row, int v, int V,
   }
 }
 
-// A request's folded Philox constants (philox_fold).
+// A request's folded Philox constants (philox_fold), its flags and its
+// temperature, read once per CTA.
 struct alignas(16) RowNoise {
   uint4 pre;
   uint4 rk[4];
+  uint32_t pad;     // a padding row: l = bias
+  uint32_t greedy;  // a greedy request
+  float T;
+  uint32_t unused;
 };
 
 // kMinBlocks: 2 where the shared memory lets two CTAs share an SM (the
@@ -143,6 +148,9 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
     philox_fold(noise_s[bl].pre, noise_s[bl].rk, (uint32_t)sd, (uint32_t)(sd >> 32),
                 (uint32_t)k | ((uint32_t)kNoiseDraft << 16), (uint32_t)off,
                 (uint32_t)(off >> 32));
+    noise_s[bl].pad = a.pad_row != nullptr && a.pad_row[g0 + bl] != 0;
+    noise_s[bl].greedy = a.greedy != nullptr && a.greedy[g0 + bl] != 0;
+    noise_s[bl].T = request_temperature(a, g0 + bl);
   }
 
   SampleState st[kRowsPerWarp];
@@ -185,7 +193,7 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
         const int bl = warp + kWarps * (p + q);
 #pragma unroll
         for (int e = 0; e < 4; ++e) base4[q][e] = 0.0f;
-        if (bl < nb && !(a.pad_row != nullptr && a.pad_row[g0 + bl] != 0))
+        if (bl < nb && !noise_s[bl].pad)
           load_base4<BT, kVec>(base + ((size_t)(g0 + bl) * K + k) * V, v0 + 4 * lane, V,
                                base4[q]);
       }
@@ -221,10 +229,10 @@ position_generic_kernel(DraftArgs a, int k, int tiles_per_chunk) {
         if (bl >= nb) break;
         const int b = g0 + bl;
         const size_t row = (size_t)b * K + k;
-        const bool pad = a.pad_row != nullptr && a.pad_row[b] != 0;
-        const bool greedy = a.greedy != nullptr && a.greedy[b] != 0;
+        const bool pad = noise_s[bl].pad != 0;
+        const bool greedy = noise_s[bl].greedy != 0;
         float l[4];
-        const float T = request_temperature(a, b);
+        const float T = noise_s[bl].T;
 #pragma unroll
         for (int e = 0; e < 4; ++e) l[e] = pad ? acc[q][e] : __fadd_rn(base4[q][e], acc[q][e]);
         store_logits4<kVec>(a.logits + row * V, v, V, l);
