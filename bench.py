@@ -473,6 +473,12 @@ def run_ours(args, rank, world):
         dist.init_process_group("nccl")
 
     w = wl.make_config(args.config if args.mode == "ncu" else CONFIG_ID)
+    if args.mode == "ncu" and args.f32_head_rank > 0:
+        # the same requests and drafter logits, a float32 head of that rank
+        rng = np.random.default_rng(7000 + args.f32_head_rank)
+        w.r = args.f32_head_rank
+        w.U = rng.standard_normal((w.V, w.r), dtype=np.float32) * np.float32(0.02)
+        w.Wb = rng.standard_normal((w.r, w.V), dtype=np.float32) * np.float32(0.02)
     if args.positions != w.K:
         w.K = args.positions
         w.base = np.ascontiguousarray(w.base[:, :w.K])
@@ -761,6 +767,9 @@ def main():
     ap.add_argument("--ncu-extra", action="store_true",
                     help="--mode ncu: also one call of each verification "
                          "rule and of the target sampler")
+    ap.add_argument("--f32-head-rank", type=int, default=0,
+                    help="--mode ncu: the workload's shape with a float32 "
+                         "head of this rank (the FFMA position kernel)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
